@@ -1,0 +1,134 @@
+"""Float64 CPU oracle for scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The CUDA library never
+imports this package and this package never imports the CUDA library.
+
+The arithmetic lives in ``attention_oracle.c`` (plain C, float64, one query
+row at a time, three stages: scores, max-subtracted softmax, weighted sum of
+V).  This module only compiles that file with gcc and marshals numpy arrays.
+
+Citations for each stage are in the C file's header: "第 11 章 · Attention
+入门" §11.1/§11.3/§11.8.1 and "3.3 Self-Attention机制深入理解" §3, §7.2, §9.3,
+§10.2.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attention_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_build/liboracle.so``; return its path."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class OracleLib:
+    """A loaded copy of the C oracle (``path`` defaults to the built library)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        fn = lib.attn_oracle_f64
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_int,
+        ]
+        self._lib = lib
+        self.path = path
+
+    def attention_f64(self, q, k, v, causal: bool, scale: float | None = None,
+                      rows=None, nthreads: int | None = None):
+        """Return ``(o, lse)`` in float64.
+
+        q: [B, Hq, Tq, D]; k, v: [B, Hkv, Tk, D] (numpy or CPU torch, any
+        float dtype; values are widened to float32, which is exact for
+        bf16/fp16/fp32).  ``scale`` defaults to 1/sqrt(D) ("第 11 章 ·
+        Attention 入门" §11.1).  ``rows``: optional flat row indices
+        ``(b*Hq + h)*Tq + i``; then ``o`` is [len(rows), D] and ``lse`` is
+        [len(rows)].  Otherwise ``o`` is [B, Hq, Tq, D] and ``lse`` is
+        [B, Hq, Tq].  ``lse`` is the natural-log log-sum-exp of the scaled,
+        masked scores.
+        """
+        q = _as_f32(q)
+        k = _as_f32(k)
+        v = _as_f32(v)
+        if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+            raise ValueError("q, k, v must be 4-D [B, H, T, D]")
+        B, Hq, Tq, D = q.shape
+        Bk, Hkv, Tk, Dk = k.shape
+        if k.shape != v.shape or Bk != B or Dk != D:
+            raise ValueError("shape mismatch between q, k and v")
+        if scale is None:
+            scale = 1.0 / np.sqrt(D)
+        if rows is not None:
+            rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+            n = rows.shape[0]
+            o = np.empty((n, D), dtype=np.float64)
+            lse = np.empty((n,), dtype=np.float64)
+            rows_ptr, nrows = rows.ctypes.data, n
+        else:
+            o = np.empty((B, Hq, Tq, D), dtype=np.float64)
+            lse = np.empty((B, Hq, Tq), dtype=np.float64)
+            rows_ptr, nrows = None, 0
+        rc = self._lib.attn_oracle_f64(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, Tq, Tk, D,
+            1 if causal else 0, float(scale), rows_ptr, nrows, o.ctypes.data,
+            lse.ctypes.data, int(nthreads or default_threads()))
+        if rc != 0:
+            raise ValueError(f"attn_oracle_f64 failed with code {rc}")
+        return o, lse
+
+
+def _load() -> OracleLib:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = OracleLib(_LIB_PATH)
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return max(1, os.cpu_count() or 1)
+
+
+def attention_f64(q, k, v, causal: bool, scale: float | None = None,
+                  rows=None, nthreads: int | None = None):
+    """Float64 attention of the built oracle; see ``OracleLib.attention_f64``."""
+    return _load().attention_f64(q, k, v, causal, scale, rows, nthreads)
+
+
+def _as_f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu")
+        import torch  # local: torch is optional for numpy callers
+        x = x.to(torch.float32).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
