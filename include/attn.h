@@ -1,0 +1,126 @@
+/*
+ * attn.h -- C ABI of libattn.so: scaled dot-product attention forward on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("第 11 章 · Attention 入门" §11.1; "3.3 Self-Attention机制深入理解"
+ * §3.6, complete formula):
+ *
+ *     O = softmax(Q K^T * scale + mask) V
+ *
+ * evaluated per (batch b, query head hq) with key/value head
+ * hkv = hq / (Hq / Hkv) ("Attention 入门" §11.8.1 MHA/MQA/GQA; "Self-Attention
+ * 机制深入理解" §9.3).  With causal != 0, query row i sees key j iff
+ * j <= i + (Tk - Tq): the lower-triangular mask of "Self-Attention机制深入理解"
+ * §10.2 when Tq == Tk, aligned so the last query sees the last key otherwise.
+ * The score matrix is never written to memory: the kernels tile Q and K/V and
+ * keep a running row max and sum ("Self-Attention机制深入理解" §7.3, §12.2,
+ * §12.3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory: q, k, v, o and lse are DEVICE pointers owned by the caller; the
+ *   library keeps none of them after the call returns.
+ * Layout: q and o are [B, Hq, Tq, D], k and v are [B, Hkv, Tk, D], row-major
+ *   and contiguous, D innermost.  lse is float32 [B, Hq, Tq], or NULL when not
+ *   wanted.  q, k, v, o must be 16-byte aligned; lse 4-byte aligned.
+ * Element type: q, k, v and o share one type (attn_dtype); accumulation is
+ *   always float32 ("Attention 入门" §11.8.5: 16-bit I/O, fp32 accumulation).
+ * lse: natural-log log-sum-exp of the row's scaled, masked scores,
+ *   lse_i = ln sum_j exp(scale * q_i . k_j).
+ * Supported: B, Hq, Hkv, Tq, Tk >= 1; D in {64, 128}; Hq % Hkv == 0;
+ *   causal requires Tq <= Tk; scale finite.  Element counts must fit in
+ *   64-bit, Tq and Tk below 2^31.
+ * Streams: every call is asynchronous on `stream` (0 = legacy default
+ *   stream).  Argument errors are returned synchronously before anything is
+ *   launched.  A launch failure returns ATTN_ERR_CUDA.  Errors raised while
+ *   the kernel runs (a pipeline wait that ran out of time) are recorded in a
+ *   device status word that attn_get_device_status reads.
+ * Threads: entry points may be called from several host threads; the
+ *   message of attn_last_error is per thread.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* bad pointer, shape, alignment or scale */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (e.g. D) */
+    ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    ATTN_ERR_NO_MEMORY = 4,   /* workspace allocation failed */
+    ATTN_ERR_TIMEOUT = 5      /* a kernel pipeline wait ran out of time */
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- attention forward, dispatching on dtype and Tq.
+ *   ATTN_BF16, Tq == 1 -> split-KV decode (attn_fwd_decode, automatic split
+ *                         count; "Attention 入门" §11.8.2: decode streams
+ *                         K/V from the cache with a 1 x N query).
+ *   ATTN_BF16, Tq >= 2 -> tensor-core prefill (attn_fwd_prefill).
+ *   ATTN_F32           -> float32 tiled kernel on the CUDA cores.
+ * scale multiplies the raw dot products; callers normally pass 1/sqrt(D)
+ * ("Attention 入门" §11.1; "Self-Attention机制深入理解" §3.3, §6).
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o,
+                     float* lse, int B, int Hq, int Hkv, int Tq, int Tk, int D,
+                     int causal, float scale, attn_dtype dtype,
+                     cudaStream_t stream);
+
+/*
+ * attn_fwd_prefill -- bf16 tiled attention on the 5th-generation tensor cores
+ * ("Self-Attention机制深入理解" §12.2 tiling with §12.3 online softmax; causal
+ * tiles wholly above the diagonal are skipped and the diagonal tile is masked
+ * element-wise, "Attention 入门" §11.8.3).  Any Tq >= 1.  q, k, v, o are
+ * bf16 (uint16 storage).  Same arguments and errors as attn_fwd.
+ */
+attn_status attn_fwd_prefill(const void* q, const void* k, const void* v,
+                             void* o, float* lse, int B, int Hq, int Hkv,
+                             int Tq, int Tk, int D, int causal, float scale,
+                             cudaStream_t stream);
+
+/*
+ * attn_fwd_decode -- one query row per (b, hq) against a contiguous KV cache
+ * (Tq == 1, so the causal mask keeps every key).  q, o: [B, Hq, 1, D] bf16;
+ * k, v: [B, Hkv, Tk, D] bf16.  The keys of each (b, hkv) are cut into
+ * num_splits contiguous ranges processed in parallel; each range yields a
+ * normalised partial output and its log-sum-exp, merged afterwards with the
+ * block-merge rule of "Self-Attention机制深入理解" §12.3.
+ * num_splits: 0 = choose from B*Hkv and the SM count; otherwise 1..256
+ * (clamped to the number of keys).  The result does not depend on the split
+ * count beyond float32 rounding.  Partial results live in a workspace the
+ * library allocates and frees on `stream` (stream-ordered); a failed
+ * allocation returns ATTN_ERR_NO_MEMORY.
+ */
+attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
+                            void* o, float* lse, int B, int Hq, int Hkv,
+                            int Tk, int D, float scale, int num_splits,
+                            cudaStream_t stream);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then read and clear the
+ * device status word of the current device.  Returns ATTN_ERR_TIMEOUT when a
+ * kernel gave up on a pipeline wait since the last call (its outputs are
+ * then undefined), ATTN_ERR_CUDA when synchronising failed, else ATTN_OK.
+ */
+attn_status attn_get_device_status(cudaStream_t stream);
+
+/* Message describing the last error returned on this host thread ("" if none).
+ * The pointer stays valid until the next call on the same thread. */
+const char* attn_last_error(void);
+
+/* Number of work items (CTAs' worth of tiles) the last prefill call on this
+ * thread scheduled and the grid it used; for tests and the bench. */
+void attn_last_launch_info(int* grid, int* items, int* kernels_launched);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

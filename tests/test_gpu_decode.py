@@ -1,0 +1,57 @@
+"""Split-KV decode parity against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, compare, to_dev
+from transformer_attention_fwd_gb300.inputs import WORKLOADS, make_qkv, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_gqa_decode_full(seed):
+    """B=64, Hq=32, Hkv=8, Tk=4096, D=128: every output compared."""
+    a = attn()
+    w = WORKLOADS["gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128"]
+    q, k, v = make_workload(w, seed)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=False)
+    check_status(a)
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, w.name)
+
+
+def test_split_count_does_not_change_result():
+    a = attn()
+    q, k, v = to_dev(*make_qkv(4, 8, 2, 1, 3000, 128, "bf16", seed=3))
+    ref_o, ref_l = a.attn_fwd_decode(q, k, v, num_splits=1)
+    for s in (2, 3, 4, 8, 16, 64):
+        o, l = a.attn_fwd_decode(q, k, v, num_splits=s)
+        assert (o.float() - ref_o.float()).abs().max().item() <= 8e-3, s
+        assert (l - ref_l).abs().max().item() <= 2e-5, s
+    check_status(a)
+
+
+def test_decode_equals_prefill_kernel_at_tq1():
+    a = attn()
+    q, k, v = to_dev(*make_qkv(2, 8, 4, 1, 777, 128, "bf16", seed=4))
+    o1, l1 = a.attn_fwd_decode(q, k, v)
+    o2, l2 = a.attn_fwd_prefill(q, k, v, causal=True)
+    check_status(a)
+    assert (o1.float() - o2.float()).abs().max().item() <= 8e-3
+    assert (l1 - l2).abs().max().item() <= 5e-5
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tk,D,splits", [
+    (1, 1, 1, 1, 64, 0), (3, 4, 4, 7, 64, 0), (2, 32, 1, 1000, 128, 0),  # MHA tiny, MQA
+    (2, 16, 2, 4097, 128, 0), (1, 8, 8, 513, 64, 5), (2, 12, 4, 129, 128, 1),
+    (1, 6, 2, 2000, 64, 7),
+])
+def test_decode_shapes(B, Hq, Hkv, Tk, D, splits):
+    a = attn()
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=Tk)
+    o, lse = a.attn_fwd_decode(*to_dev(q, k, v), num_splits=splits)
+    check_status(a)
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)

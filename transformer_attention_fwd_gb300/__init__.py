@@ -5,14 +5,12 @@
 """
 from __future__ import annotations
 
-__all__ = ["attn", "inputs"]
+import importlib
+
+__all__ = ["attn", "inputs", "build"]
 
 
 def __getattr__(name):
-    if name == "attn":
-        from . import attn as _attn
-        return _attn
-    if name == "inputs":
-        from . import inputs as _inputs
-        return _inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

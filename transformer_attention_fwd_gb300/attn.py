@@ -1,0 +1,188 @@
+"""ctypes binding over libattn.so (include/attn.h, include/attn_diag.h).
+
+Argument marshalling only: the functions check tensor placement, dtype and
+contiguity, allocate outputs with torch, and pass raw device pointers plus the
+current CUDA stream to the C ABI.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.  If the library is missing the
+import-time load raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_NO_MEMORY = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_F32 = 0
+ATTN_BF16 = 1
+
+STATUS_NAMES = {
+    ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
+    ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED", ATTN_ERR_CUDA: "ATTN_ERR_CUDA",
+    ATTN_ERR_NO_MEMORY: "ATTN_ERR_NO_MEMORY", ATTN_ERR_TIMEOUT: "ATTN_ERR_TIMEOUT",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with transformer_attention_fwd_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F, LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+    sig = {
+        "attn_fwd": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
+        "attn_fwd_prefill": [P, P, P, P, P, I, I, I, I, I, I, I, F, P],
+        "attn_fwd_decode": [P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "attn_get_device_status": [P],
+        "attn_diag_mma_tile": [P, P, P, P, P, I, P],
+        "attn_diag_wait_timeout": [LL, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_last_launch_info.argtypes = [ctypes.POINTER(I)] * 3
+    lib.attn_last_launch_info.restype = None
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.attn_last_error().decode("utf-8", "replace")
+
+
+def _check(status: int) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, last_error())
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def last_launch_info():
+    g, i, k = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    lib.attn_last_launch_info(ctypes.byref(g), ctypes.byref(i), ctypes.byref(k))
+    return g.value, i.value, k.value
+
+
+def _shapes(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, T, D]")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [B, H, T, D]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    B, Hq, Tq, D = q.shape
+    Bk, Hkv, Tk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("k and v must be [B, Hkv, Tk, D] with q's B and D")
+    return B, Hq, Hkv, Tq, Tk, D
+
+
+def _outputs(q, out, lse, want_lse):
+    B, Hq, Tq, D = q.shape
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    return o, lse
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """O = softmax(Q K^T * scale + causal mask) V through ``attn_fwd``.
+
+    q: [B, Hq, Tq, D], k/v: [B, Hkv, Tk, D], all fp32 or all bf16 CUDA tensors.
+    Returns ``(o, lse)``; ``lse`` (fp32 [B, Hq, Tq]) is None if not wanted.
+    ``scale`` defaults to 1/sqrt(D).
+    """
+    B, Hq, Hkv, Tq, Tk, D = _shapes(q, k, v)
+    if q.dtype == torch.float32:
+        dt = ATTN_F32
+    elif q.dtype == torch.bfloat16:
+        dt = ATTN_BF16
+    else:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o, lse = _outputs(q, out, lse, want_lse)
+    _check(lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk, D,
+                        1 if causal else 0, scale, dt, _stream_handle(stream)))
+    return o, lse
+
+
+def attn_fwd_prefill(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                     lse=None, want_lse: bool = True, stream=None):
+    """The bf16 tensor-core path for any Tq (``attn_fwd_prefill``)."""
+    B, Hq, Hkv, Tq, Tk, D = _shapes(q, k, v)
+    if q.dtype != torch.bfloat16:
+        raise ValueError("attn_fwd_prefill takes bf16 tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o, lse = _outputs(q, out, lse, want_lse)
+    _check(lib.attn_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq,
+                                Tk, D, 1 if causal else 0, scale, _stream_handle(stream)))
+    return o, lse
+
+
+def attn_fwd_decode(q, k, v, scale: float | None = None, num_splits: int = 0, out=None,
+                    lse=None, want_lse: bool = True, stream=None):
+    """Split-KV decode (``attn_fwd_decode``): q [B, Hq, 1, D] bf16 against
+    k/v [B, Hkv, Tk, D]; ``num_splits`` 0 = automatic."""
+    B, Hq, Hkv, Tq, Tk, D = _shapes(q, k, v)
+    if Tq != 1:
+        raise ValueError("decode takes one query row per (b, hq)")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("attn_fwd_decode takes bf16 tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o, lse = _outputs(q, out, lse, want_lse)
+    _check(lib.attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tk, D,
+                               scale, int(num_splits), _stream_handle(stream)))
+    return o, lse
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status as an
+    attn_status code (ATTN_ERR_TIMEOUT if a kernel wait ran out of time)."""
+    return lib.attn_get_device_status(_stream_handle(stream))
+
+
+def diag_mma_tile(a, b, v, stream=None):
+    """Self-test of the tensor-core tile products; returns (s, o) fp32."""
+    D = a.shape[1]
+    s = torch.empty((128, 128), dtype=torch.float32, device=a.device)
+    o = torch.empty((128, D), dtype=torch.float32, device=a.device)
+    _check(lib.attn_diag_mma_tile(_ptr(a), _ptr(b), _ptr(v), _ptr(s), _ptr(o), D,
+                                  _stream_handle(stream)))
+    return s, o
+
+
+def diag_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib.attn_diag_wait_timeout(int(timeout_ns), _stream_handle(stream)))

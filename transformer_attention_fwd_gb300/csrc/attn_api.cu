@@ -1,0 +1,387 @@
+// attn_api.cu -- the C ABI of libattn.so (declared in include/attn.h and
+// include/attn_diag.h): argument validation, dispatch, TMA tensor maps, the
+// decode workspace and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/attn.h"
+#include "../../include/attn_diag.h"
+#include "attn_internal.h"
+
+namespace attn {
+
+// Device status word: kernels OR error bits into it (see sm100.cuh).
+__device__ unsigned g_attn_status;
+
+namespace {
+
+thread_local std::string t_last_error;
+thread_local int t_last_grid = 0, t_last_items = 0, t_last_kernels = 0;
+
+attn_status fail(attn_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return st;
+}
+
+attn_status ok() {
+    t_last_error.clear();
+    return ATTN_OK;
+}
+
+attn_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Per-device facts gathered once.
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned* status = nullptr;
+};
+std::mutex g_dev_mutex;
+DeviceState g_dev[64];
+
+constexpr uint64_t kWaitLimitNs = 2ull * 1000ull * 1000ull * 1000ull;  // 2 s per wait
+
+attn_status device_env(cudaStream_t stream, LaunchEnv* env) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        DeviceState& d = g_dev[dev];
+        if (!d.ready) {
+            cudaDeviceProp prop;
+            e = cudaGetDeviceProperties(&prop, dev);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+            d.num_sms = prop.multiProcessorCount;
+            d.cc_major = prop.major;
+            d.cc_minor = prop.minor;
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_attn_status);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+            d.status = static_cast<unsigned*>(p);
+            d.ready = true;
+        }
+        if (!(d.cc_major == 10 && d.cc_minor == 3))
+            return fail(ATTN_ERR_UNSUPPORTED,
+                        "libattn.so is built for sm_103a; device %d has compute capability %d.%d",
+                        dev, d.cc_major, d.cc_minor);
+        env->num_sms = d.num_sms;
+        env->status = d.status;
+    }
+    env->device = dev;
+    env->stream = stream;
+    env->wait_limit_ns = kWaitLimitNs;
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Validation
+// ---------------------------------------------------------------------------
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn_status validate(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     int B, int Hq, int Hkv, int Tq, int Tk, int D, int causal, float scale) {
+    if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (lse && !aligned(lse, 4)) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+    if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || D < 1)
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "B, Hq, Hkv, Tq, Tk, D must be >= 1 (got %d, %d, %d, %d, %d, %d)", B, Hq, Hkv,
+                    Tq, Tk, D);
+    if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim D=%d not supported (64 or 128)", D);
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    if (causal && Tq > Tk)
+        return fail(ATTN_ERR_INVALID_ARG, "causal attention needs Tq <= Tk (got Tq=%d, Tk=%d)", Tq, Tk);
+    if (!std::isfinite(scale) || !(scale > 0.0f))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and positive (got %g)", (double)scale);
+    const long long bh = static_cast<long long>(B) * Hq, bkv = static_cast<long long>(B) * Hkv;
+    if (bh > 0x7fffffffLL || bkv > 0x7fffffffLL)
+        return fail(ATTN_ERR_INVALID_ARG, "B*Hq and B*Hkv must fit in 31 bits");
+    if (Tq > 0x7fffffffLL - 1024 || Tk > 0x7fffffffLL - 1024)
+        return fail(ATTN_ERR_INVALID_ARG, "Tq and Tk must be below 2^31 - 1024");
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// TMA tensor maps ([rows][D] bf16 slabs stacked over batch*heads), cached.
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    long long rows, slabs;
+    int D, box_rows, rank;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && rows == o.rows && slabs == o.slabs && D == o.D &&
+               box_rows == o.box_rows && rank == o.rank;
+    }
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+};
+std::mutex g_map_mutex;
+std::vector<MapEntry> g_maps;  // most recently used last
+constexpr size_t kMapCacheSize = 64;
+
+// Tiled map over a [slabs][rows][D] bf16 tensor; box = 64 columns x box_rows
+// rows x 1 slab, 128-byte swizzle, zero fill outside the tensor.
+attn_status make_map(const void* ptr, long long rows, long long slabs, int D, int box_rows,
+                     int rank, CUtensorMap* out) {
+    const MapKey key{ptr, rows, slabs, D, box_rows, rank};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (size_t i = g_maps.size(); i-- > 0;) {
+            if (g_maps[i].key == key) {
+                *out = g_maps[i].map;
+                if (i + 1 != g_maps.size()) {
+                    MapEntry e = g_maps[i];
+                    g_maps.erase(g_maps.begin() + static_cast<long>(i));
+                    g_maps.push_back(e);
+                }
+                return ATTN_OK;
+            }
+        }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(slabs)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                             static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(rows)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUtensorMap m;
+    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                    const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        if (g_maps.size() >= kMapCacheSize) g_maps.erase(g_maps.begin());
+        g_maps.push_back(MapEntry{key, m});
+    }
+    *out = m;
+    return ATTN_OK;
+}
+
+void record_launch(int grid, int items, int kernels) {
+    t_last_grid = grid;
+    t_last_items = items;
+    t_last_kernels = kernels;
+}
+
+attn_status run_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const Shape& s, const LaunchEnv& env) {
+    PrefillMaps maps;
+    const int box = prefill_box_rows();
+    attn_status st = make_map(q, s.Tq, static_cast<long long>(s.B) * s.Hq, s.D, box, 3, &maps.q);
+    if (st != ATTN_OK) return st;
+    st = make_map(k, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.k);
+    if (st != ATTN_OK) return st;
+    st = make_map(v, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.v);
+    if (st != ATTN_OK) return st;
+    int grid = 0, items = 0, kernels = 0;
+    cudaError_t e = launch_prefill_bf16(maps, static_cast<uint16_t*>(o), lse, s, env, &grid,
+                                        &items, &kernels);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    record_launch(grid, items, kernels);
+    return ok();
+}
+
+attn_status run_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                       const Shape& s, int num_splits, const LaunchEnv& env) {
+    int splits = num_splits > 0 ? num_splits : decode_choose_splits(s, env.num_sms);
+    if (splits > 256) splits = 256;
+    if (splits > s.Tk) splits = s.Tk;
+    // Recompute so that no split is empty.
+    const int per = (s.Tk + splits - 1) / splits;
+    splits = (s.Tk + per - 1) / per;
+
+    float* ws_o = nullptr;
+    float* ws_lse = nullptr;
+    void* ws = nullptr;
+    if (splits > 1) {
+        const size_t bytes = decode_workspace_bytes(s, splits);
+        cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
+        if (e != cudaSuccess || ws == nullptr) {
+            cudaGetLastError();
+            return fail(ATTN_ERR_NO_MEMORY, "decode workspace of %zu bytes: %s", bytes,
+                        cudaGetErrorString(e));
+        }
+        ws_o = static_cast<float*>(ws);
+        const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+        ws_lse = ws_o + rows * splits * s.D;
+    }
+    int kernels = 0;
+    cudaError_t e = launch_decode_bf16(static_cast<const uint16_t*>(q),
+                                       static_cast<const uint16_t*>(k),
+                                       static_cast<const uint16_t*>(v), static_cast<uint16_t*>(o),
+                                       lse, ws_o, ws_lse, s, splits, env, &kernels);
+    if (ws) {
+        cudaError_t f = cudaFreeAsync(ws, env.stream);
+        if (e == cudaSuccess && f != cudaSuccess) e = f;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    record_launch(s.B * s.Hkv, splits, kernels);
+    return ok();
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status attn_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Tq, int Tk, int D, int causal,
+                             float scale, cudaStream_t stream) {
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, causal, scale);
+    if (st != ATTN_OK) return st;
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    const Shape s{B, Hq, Hkv, Tq, Tk, D, causal ? 1 : 0, scale};
+    return run_prefill(q, k, v, o, lse, s, env);
+}
+
+attn_status attn_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Tk, int D, float scale, int num_splits,
+                            cudaStream_t stream) {
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, 1, Tk, D, 0, scale);
+    if (st != ATTN_OK) return st;
+    if (num_splits < 0 || num_splits > 256)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in 0..256 (got %d)", num_splits);
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    const Shape s{B, Hq, Hkv, 1, Tk, D, 0, scale};
+    return run_decode(q, k, v, o, lse, s, num_splits, env);
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Tq, int Tk, int D, int causal, float scale,
+                     attn_dtype dtype, cudaStream_t stream) {
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, causal, scale);
+    if (st != ATTN_OK) return st;
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    const Shape s{B, Hq, Hkv, Tq, Tk, D, causal ? 1 : 0, scale};
+    if (dtype == ATTN_F32) {
+        int kernels = 0;
+        cudaError_t e = launch_simt_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                        s, env, &kernels);
+        if (e == cudaErrorInvalidConfiguration)
+            return fail(ATTN_ERR_UNSUPPORTED, "Tq=%d too long for the fp32 kernel's grid", Tq);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 launch");
+        record_launch(B * Hq, (Tq + 15) / 16, kernels);
+        return ok();
+    }
+    if (Tq == 1) return run_decode(q, k, v, o, lse, s, 0, env);
+    return run_prefill(q, k, v, o, lse, s, env);
+}
+
+attn_status attn_get_device_status(cudaStream_t stream) {
+    LaunchEnv env;
+    attn_status st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, env.status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (word != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(env.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+    }
+    if (word & 1u)
+        return fail(ATTN_ERR_TIMEOUT, "a kernel pipeline wait timed out (site %u); outputs undefined",
+                    (word >> 8) & 0xffu);
+    return ok();
+}
+
+const char* attn_last_error(void) { return t_last_error.c_str(); }
+
+void attn_last_launch_info(int* grid, int* items, int* kernels_launched) {
+    if (grid) *grid = t_last_grid;
+    if (items) *items = t_last_items;
+    if (kernels_launched) *kernels_launched = t_last_kernels;
+}
+
+attn_status attn_diag_mma_tile(const void* a, const void* b, const void* v, float* s_out,
+                               float* o_out, int D, cudaStream_t stream) {
+    if (!a || !b || !v || !s_out || !o_out)
+        return fail(ATTN_ERR_INVALID_ARG, "all pointers must be non-null");
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(v, 16))
+        return fail(ATTN_ERR_INVALID_ARG, "a, b, v must be 16-byte aligned");
+    if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "D must be 64 or 128");
+    LaunchEnv env;
+    attn_status st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    CUtensorMap ma, mb, mv;
+    if ((st = make_map(a, 128, 1, D, 128, 2, &ma)) != ATTN_OK) return st;
+    if ((st = make_map(b, 128, 1, D, 128, 2, &mb)) != ATTN_OK) return st;
+    if ((st = make_map(v, 128, 1, D, 128, 2, &mv)) != ATTN_OK) return st;
+    cudaError_t e = launch_diag_mma_tile(ma, mb, mv, s_out, o_out, D, env);
+    if (e != cudaSuccess) return cuda_fail(e, "diag mma tile launch");
+    record_launch(1, 1, 1);
+    return ok();
+}
+
+attn_status attn_diag_wait_timeout(long long timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10LL * 1000 * 1000 * 1000)
+        return fail(ATTN_ERR_INVALID_ARG, "timeout_ns must be in [1e3, 1e10]");
+    LaunchEnv env;
+    attn_status st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = launch_diag_wait_timeout(env, static_cast<uint64_t>(timeout_ns));
+    if (e != cudaSuccess) return cuda_fail(e, "diag wait launch");
+    record_launch(1, 1, 1);
+    return ok();
+}
+
+}  // extern "C"

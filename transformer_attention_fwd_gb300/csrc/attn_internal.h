@@ -1,0 +1,59 @@
+// attn_internal.h -- host-side interface between the C-ABI layer (attn_api.cu)
+// and the per-kernel launchers.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Everything a launcher needs besides the tensors.
+struct LaunchEnv {
+    cudaStream_t stream;
+    unsigned* status;      // device status word (see sm100.cuh)
+    uint64_t wait_limit_ns;
+    int num_sms;
+    int device;
+};
+
+struct Shape {
+    int B, Hq, Hkv, Tq, Tk, D;
+    int causal;
+    float scale;
+};
+
+// Each launcher returns cudaSuccess or the CUDA error of its launch; argument
+// validation has been done by the caller.
+cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, float* o,
+                            float* lse, const Shape& s, const LaunchEnv& env,
+                            int* kernels_launched);
+
+// Prefill on tensor cores.  Tensor maps are built by the caller.
+struct PrefillMaps {
+    CUtensorMap q, k, v;
+};
+cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse,
+                                const Shape& s, const LaunchEnv& env, int* grid_out,
+                                int* items_out, int* kernels_launched);
+int prefill_block_rows();  // query rows per CTA work item
+int prefill_box_rows();    // rows of one TMA box (Q, K and V tiles)
+
+// Split-KV decode.  ws_o: [B*Hq, splits, D] fp32, ws_lse: [B*Hq, splits] fp32
+// (log2 domain); unused (may be null) when splits == 1.
+cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               uint16_t* o, float* lse, float* ws_o, float* ws_lse,
+                               const Shape& s, int splits, const LaunchEnv& env,
+                               int* kernels_launched);
+int decode_choose_splits(const Shape& s, int num_sms);
+size_t decode_workspace_bytes(const Shape& s, int splits);
+
+// Diagnostics.
+cudaError_t launch_diag_mma_tile(const CUtensorMap& a, const CUtensorMap& b,
+                                 const CUtensorMap& v, float* s_out, float* o_out, int D,
+                                 const LaunchEnv& env);
+cudaError_t launch_diag_wait_timeout(const LaunchEnv& env, uint64_t limit_ns);
+
+}  // namespace attn

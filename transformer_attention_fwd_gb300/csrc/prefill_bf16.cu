@@ -1,0 +1,715 @@
+// prefill_bf16.cu -- bf16 attention forward on the 5th-generation tensor
+// cores (tcgen05), fp32 accumulation in tensor memory.
+//
+// The method is the tiled attention with online softmax of
+// "3.3 Self-Attention机制深入理解" §12.2/§12.3: for every tile of query rows
+// walk the key/value tiles, compute S = Q K^T, fold S into a running row
+// maximum and row sum, and accumulate P V, so the score matrix never leaves
+// the SM.  Causal tiles wholly above the diagonal are never visited and only
+// tiles that straddle the diagonal (or the end of the keys) are masked element
+// by element ("第 11 章 · Attention 入门" §11.8.3).  Query head hq reads K/V head
+// hq / (Hq / Hkv) (§11.8.1).
+//
+// GB300 mapping (one persistent CTA per SM, 384 threads):
+//   warp 0      TMA producer for Q and K tiles        (one elected lane)
+//   warp 3      TMA producer for V tiles              (one elected lane)
+//   warp 1      MMA issuer                            (one elected lane)
+//   warp 2      tensor-memory allocator
+//   warps 4-7   softmax warpgroup for query tile 0    (thread = row = TMEM lane)
+//   warps 8-11  softmax warpgroup for query tile 1
+// A work item is 256 query rows (two 128-row tiles) of one (b, hq).  Tensor
+// memory (512 columns x 128 lanes x 32 bit) holds S0, S1 (128 columns each),
+// O0, O1 (D columns each).  P overwrites the first 64 columns of its S tile as
+// packed bf16 and feeds the P.V MMA straight from tensor memory.  The MMA
+// issue order per key tile j is
+//     S0(j)  PV1(j-1)  S1(j)  PV0(j)
+// so each softmax warpgroup works on one tile while the tensor core runs the
+// other tile's products.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "sm100.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;                  // query rows per tile = TMEM lanes
+constexpr int BN = 128;                  // keys per K/V tile
+constexpr int NQT = 2;                   // query tiles per work item
+constexpr int kItemRows = BM * NQT;
+constexpr int kThreads = 384;
+constexpr int kBoxCols = 64;             // 64 bf16 = one 128-byte swizzle row
+constexpr int kBoxBytes = kBoxCols * BM * 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Wait sites reported in the status word when a wait times out.
+enum : unsigned {
+    SITE_Q_EMPTY = 1, SITE_K_EMPTY, SITE_V_EMPTY, SITE_Q_FULL, SITE_K_FULL, SITE_V_FULL,
+    SITE_P_FULL, SITE_O_EMPTY, SITE_S_FULL, SITE_O_FULL, SITE_DIAG_LOAD, SITE_DIAG_MMA,
+    SITE_DIAG_TIMEOUT
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / kBoxCols;
+    static constexpr int kTileBytes = kChunks * kBoxBytes;  // 128 rows x D bf16
+    static constexpr int kKStages = (D == 128) ? 3 : 4;
+    static constexpr int kVStages = (D == 128) ? 2 : 4;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + NQT * kTileBytes;
+    static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + 1024-byte alignment slack
+    // Tensor-memory columns of the S/P and O accumulators of query tile t.
+    __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+    __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+};
+
+struct Bars {
+    uint64_t q_full, q_empty;
+    uint64_t k_full[4], k_empty[4];
+    uint64_t v_full[4], v_empty[4];
+    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block too large");
+
+struct PrefillParams {
+    uint16_t* o;
+    float* lse;
+    int Hq, Hkv, Tq, Tk, group, causal;
+    float scale_log2;
+    int n_qblocks, n_bh, n_items;
+    unsigned* status;
+    unsigned long long limit_ns;
+};
+
+struct Item {
+    int bh, qb, bkv;
+    int n[2];  // key tiles visited by query tile 0 / 1 (0: tile is past Tq)
+};
+
+// Work item idx -> (bh, query block).  Query blocks are handed out from the
+// last (longest under the causal mask) to the first.
+__device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p) {
+    Item it;
+    const int qrev = idx / p.n_bh;
+    it.bh = idx - qrev * p.n_bh;
+    it.qb = p.n_qblocks - 1 - qrev;
+    const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
+    it.bkv = b * p.Hkv + hq / p.group;
+#pragma unroll
+    for (int t = 0; t < NQT; ++t) {
+        const int r0 = it.qb * kItemRows + t * BM;
+        if (r0 >= p.Tq) {
+            it.n[t] = 0;
+        } else if (p.causal) {
+            const int rlast = min(r0 + BM - 1, p.Tq - 1);
+            const int kmax = min(p.Tk - 1, rlast + (p.Tk - p.Tq));
+            it.n[t] = kmax / BN + 1;
+        } else {
+            it.n[t] = (p.Tk + BN - 1) / BN;
+        }
+    }
+    return it;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    const uint32_t s = smem_u32(p);
+    return p + ((1024u - (s & 1023u)) & 1023u);
+}
+
+// S[tmem cols] = Q_tile . K_tile^T : M = 128, N = 128, K = D in steps of 16.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = static_cast<uint32_t>((kk / 4) * kBoxBytes + (kk % 4) * 32);
+        const uint64_t a = smem_desc_sw128(q_smem + off, 16, 1024);
+        const uint64_t b = smem_desc_sw128(k_smem + off, 16, 1024);
+        mma_bf16_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
+// P is read from tensor memory (8 columns per 16 keys); V is MN-major.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true);
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        const uint64_t b = smem_desc_sw128(v_smem + kk * 16 * 128, kBoxBytes, 1024);
+        mma_bf16_ts(o_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// Wait without recording a timeout (used only while draining after an abort).
+__device__ __forceinline__ void wait_quiet(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return;
+    }
+}
+
+constexpr uint64_t kDrainLimitNs = 200ull * 1000ull * 1000ull;
+
+// ----------------------------------------------------------------------------
+// Roles
+// ----------------------------------------------------------------------------
+template <int D>
+__device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint8_t* smem,
+                            Bars* bars, const PrefillParams& p, const WaitGuard& g) {
+    using C = Cfg<D>;
+    uint32_t kv_it = 0, q_it = 0;
+    int issued_q = 0;
+    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(idx, p);
+        const int nkv = max(it.n[0], it.n[1]);
+        if (q_it > 0 && !mbar_wait(&bars->q_empty, (q_it - 1) & 1, g, SITE_Q_EMPTY)) goto drain;
+        mbar_arrive_expect_tx(&bars->q_full,
+                              ((it.n[0] > 0) + (it.n[1] > 0)) * C::kTileBytes);
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+            if (it.n[t] == 0) continue;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, tmQ,
+                            &bars->q_full, c * kBoxCols, it.qb * kItemRows + t * BM, it.bh);
+        }
+        ++q_it;
+        issued_q = 1;
+        for (int j = 0; j < nkv; ++j, ++kv_it) {
+            const int s = kv_it % C::kKStages;
+            const uint32_t ph = (kv_it / C::kKStages) & 1;
+            if (kv_it >= C::kKStages && !mbar_wait(&bars->k_empty[s], ph ^ 1, g, SITE_K_EMPTY))
+                goto drain;
+            mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * kBoxBytes, tmK,
+                            &bars->k_full[s], c * kBoxCols, j * BN, it.bkv);
+        }
+    }
+    return;
+drain:
+    // Let copies already in flight land before the CTA leaves.
+    if (issued_q) wait_quiet(&bars->q_full, (q_it - 1) & 1, kDrainLimitNs);
+    for (uint32_t i = (kv_it > (uint32_t)C::kKStages ? kv_it - C::kKStages : 0); i < kv_it; ++i)
+        wait_quiet(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, kDrainLimitNs);
+}
+
+template <int D>
+__device__ void producer_v(const CUtensorMap* tmV, uint8_t* smem, Bars* bars,
+                           const PrefillParams& p, const WaitGuard& g) {
+    using C = Cfg<D>;
+    uint32_t kv_it = 0;
+    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(idx, p);
+        const int nkv = max(it.n[0], it.n[1]);
+        for (int j = 0; j < nkv; ++j, ++kv_it) {
+            const int s = kv_it % C::kVStages;
+            const uint32_t ph = (kv_it / C::kVStages) & 1;
+            if (kv_it >= C::kVStages && !mbar_wait(&bars->v_empty[s], ph ^ 1, g, SITE_V_EMPTY))
+                goto drain;
+            mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * kBoxBytes, tmV,
+                            &bars->v_full[s], c * kBoxCols, j * BN, it.bkv);
+        }
+    }
+    return;
+drain:
+    for (uint32_t i = (kv_it > (uint32_t)C::kVStages ? kv_it - C::kVStages : 0); i < kv_it; ++i)
+        wait_quiet(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, kDrainLimitNs);
+}
+
+template <int D>
+__device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const PrefillParams& p,
+                           const WaitGuard& g) {
+    using C = Cfg<D>;
+    const uint32_t q_base = smem_u32(smem + C::kQOff);
+    const uint32_t k_base = smem_u32(smem + C::kKOff);
+    const uint32_t v_base = smem_u32(smem + C::kVOff);
+    uint32_t kv_it = 0, q_it = 0;
+    uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+
+    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(idx, p);
+        const int n0 = it.n[0], n1 = it.n[1];
+        const int nkv = max(n0, n1);
+        if (!mbar_wait(&bars->q_full, q_it & 1, g, SITE_Q_FULL)) goto drain;
+        ++q_it;
+        tc_fence_after_sync();
+        const uint32_t first = kv_it;
+        for (int j = 0; j <= nkv; ++j) {
+            const uint32_t itj = first + j;
+            const int ks = itj % C::kKStages, vs = itj % C::kVStages;
+            const uint32_t kph = (itj / C::kKStages) & 1, vph = (itj / C::kVStages) & 1;
+            const uint32_t k_smem = k_base + ks * C::kTileBytes;
+            const uint32_t v_smem = v_base + vs * C::kTileBytes;
+            if (j < nkv) {
+                if (!mbar_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
+                tc_fence_after_sync();
+                if (j < n0) {
+                    issue_qk<D>(tmem + C::col_s(0), q_base, k_smem);
+                    mma_commit(&bars->s_full[0]);
+                }
+            }
+            if (j >= 1 && j - 1 < n1) {  // PV1(j-1)
+                const uint32_t ip = itj - 1;
+                const int pvs = ip % C::kVStages;
+                if (!mbar_wait(&bars->p_full[1], p_cnt[1] & 1, g, SITE_P_FULL)) goto drain;
+                ++p_cnt[1];
+                if (!mbar_wait(&bars->v_full[pvs], (ip / C::kVStages) & 1, g, SITE_V_FULL))
+                    goto drain;
+                if (j - 1 == 0 && o_cnt[1] > 0 &&
+                    !mbar_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
+                    goto drain;
+                tc_fence_after_sync();
+                issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
+                            v_base + pvs * C::kTileBytes, j - 1 > 0);
+                if (j - 1 == n1 - 1) {
+                    mma_commit(&bars->o_full[1]);
+                    ++o_cnt[1];
+                }
+            }
+            if (j >= 1) mma_commit(&bars->v_empty[(itj - 1) % C::kVStages]);
+            if (j < nkv) {
+                if (j < n1) {
+                    issue_qk<D>(tmem + C::col_s(1), q_base + C::kTileBytes, k_smem);
+                    mma_commit(&bars->s_full[1]);
+                }
+                mma_commit(&bars->k_empty[ks]);
+                if (j == nkv - 1) mma_commit(&bars->q_empty);
+                if (j < n0) {  // PV0(j)
+                    if (!mbar_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
+                    ++p_cnt[0];
+                    if (!mbar_wait(&bars->v_full[vs], vph, g, SITE_V_FULL)) goto drain;
+                    if (j == 0 && o_cnt[0] > 0 &&
+                        !mbar_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
+                        goto drain;
+                    tc_fence_after_sync();
+                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_smem, j > 0);
+                    if (j == n0 - 1) {
+                        mma_commit(&bars->o_full[0]);
+                        ++o_cnt[0];
+                    }
+                }
+            }
+        }
+        kv_it = first + nkv;
+    }
+drain:
+    // Wait for every MMA issued so far before tensor memory is released.
+    mma_commit(&bars->drain);
+    wait_quiet(&bars->drain, 0, kDrainLimitNs);
+}
+
+template <int D>
+__device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams& p,
+                           const WaitGuard& g) {
+    using C = Cfg<D>;
+    const int row_in_tile = threadIdx.x - 128 * (1 + t);  // = TMEM lane
+    const int warp = threadIdx.x / 32;
+    const uint32_t lane_addr = tmem_lane_base(tmem, warp);
+    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+    const int off = p.Tk - p.Tq;
+    uint32_t s_cnt = 0, o_cnt = 0;
+
+    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+        const Item it = decode_item(idx, p);
+        const int n = it.n[t];
+        if (n == 0) continue;
+        const int r0 = it.qb * kItemRows + t * BM;
+        const int row = r0 + row_in_tile;
+        // Last visible key of this row and of the tile's first row.
+        const int lim = p.causal ? min(row + off, p.Tk - 1) : p.Tk - 1;
+        const int lim_first = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
+        float m = -INFINITY, l = 0.0f;
+
+        for (int j = 0; j < n; ++j) {
+            // Warp-uniform outcome: tcgen05.ld below needs the whole warp.
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], s_cnt & 1, g, SITE_S_FULL)))
+                return;
+            ++s_cnt;
+            tc_fence_after_sync();
+            uint32_t r[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + colS + 32 * c, r[c]);
+            tmem_wait_ld(r[0]);
+            reg_order(r[1]);
+            reg_order(r[2]);
+            reg_order(r[3]);
+            const int kbase = j * BN;
+            if (kbase + BN - 1 > lim_first) {  // tile straddles the diagonal or Tk
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (kbase + 32 * c + i > lim) r[c][i] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r[c][i]));
+            const float m_new = fmaxf(m, mx * p.scale_log2);
+            const bool need = m_new > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_use = (m_new == -INFINITY) ? m : m_new;
+                const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_use);
+                l *= alpha;
+                if (j > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_addr + colO + 32 * c, ov);
+                        tmem_wait_ld(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(lane_addr + colO + 32 * c, ov);
+                    }
+                }
+                m = m_use;
+            }
+            const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+            float sum = 0.0f;
+            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i]), p.scale_log2, neg_m));
+                    const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i + 1]), p.scale_log2, neg_m));
+                    sum += a + b;
+                    r[2 * h][i] = pack_bf16x2(a, b);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i]), p.scale_log2, neg_m));
+                    const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i + 1]), p.scale_log2, neg_m));
+                    sum += a + b;
+                    r[2 * h][16 + i] = pack_bf16x2(a, b);
+                }
+            }
+            tmem_st32(lane_addr + colS, r[0]);
+            tmem_st32(lane_addr + colS + 32, r[2]);
+            tmem_wait_st();
+            l += sum;
+            tc_fence_before_sync();
+            mbar_arrive(&bars->p_full[t]);
+        }
+
+        // Epilogue: O = O_acc / l -> bf16; lse = (m + log2 l) * ln 2.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], o_cnt & 1, g, SITE_O_FULL)))
+            return;
+        ++o_cnt;
+        tc_fence_after_sync();
+        const float inv_l = 1.0f / l;
+        const bool in_range = row < p.Tq;
+        uint16_t* orow = p.o + (static_cast<int64_t>(it.bh) * p.Tq + row) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(lane_addr + colO + 32 * c, ov);
+            tmem_wait_ld(ov);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (in_range) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (in_range && p.lse != nullptr)
+            p.lse[static_cast<int64_t>(it.bh) * p.Tq + row] = (m + __log2f(l)) * kLn2;
+        tc_fence_before_sync();
+        mbar_arrive(&bars->o_empty[t]);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->p_full[t], BM);
+            mbar_init(&bars->o_full[t], 1);
+            mbar_init(&bars->o_empty[t], BM);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 2) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitGuard g{p.status, &bars->abort, p.limit_ns};
+
+    if (warp == 0) {
+        if (lane == 0) producer_qk<D>(&tmQ, &tmK, smem, bars, p, g);
+    } else if (warp == 3) {
+        if (lane == 0) producer_v<D>(&tmV, smem, bars, p, g);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer<D>(smem, bars, tmem, p, g);
+    } else if (warp >= 4) {
+        softmax_wg<D>((warp - 4) / 4, bars, tmem, p, g);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Diagnostics: one tile through the same MMA code, and a wait that times out.
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmV, float* s_out, float* o_out,
+                     unsigned* status, unsigned long long limit_ns) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    uint8_t* sa = smem;
+    uint8_t* sb = smem + C::kTileBytes;
+    uint8_t* sv = smem + 2 * C::kTileBytes;
+    Bars* bars = reinterpret_cast<Bars*>(smem + 3 * C::kTileBytes);
+    const int warp = threadIdx.x / 32;
+    const int row = threadIdx.x;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = bars->tmem_base;
+    const WaitGuard g{status, &bars->abort, limit_ns};
+    const uint32_t lane_addr = tmem_lane_base(tmem, warp);
+    bool ok = true;
+
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars->q_full, 3 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+            tma_load_2d(sa + c * kBoxBytes, &tmA, &bars->q_full, c * kBoxCols, 0);
+            tma_load_2d(sb + c * kBoxBytes, &tmB, &bars->q_full, c * kBoxCols, 0);
+            tma_load_2d(sv + c * kBoxBytes, &tmV, &bars->q_full, c * kBoxCols, 0);
+        }
+        if (mbar_wait(&bars->q_full, 0, g, SITE_DIAG_LOAD)) {
+            tc_fence_after_sync();
+            issue_qk<D>(tmem, smem_u32(sa), smem_u32(sb));
+            mma_commit(&bars->s_full[0]);
+        }
+    }
+    __syncwarp();
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], 0, g, SITE_DIAG_MMA));
+    if (ok) {
+        tc_fence_after_sync();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + 32 * c, r[c]);
+        tmem_wait_ld(r[0]);
+        reg_order(r[1]);
+        reg_order(r[2]);
+        reg_order(r[3]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s_out[row * 128 + 32 * c + i] = __uint_as_float(r[c][i]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                r[2 * h][i] = pack_bf16x2(__uint_as_float(r[2 * h][2 * i]),
+                                          __uint_as_float(r[2 * h][2 * i + 1]));
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                r[2 * h][16 + i] = pack_bf16x2(__uint_as_float(r[2 * h + 1][2 * i]),
+                                               __uint_as_float(r[2 * h + 1][2 * i + 1]));
+        }
+        tmem_st32(lane_addr, r[0]);
+        tmem_st32(lane_addr + 32, r[2]);
+        tmem_wait_st();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && ok && !bars->abort) {
+        tc_fence_after_sync();
+        issue_pv<D>(tmem + 128, tmem, smem_u32(sv), false);
+        mma_commit(&bars->s_full[0]);
+    }
+    __syncwarp();
+    ok = ok && !bars->abort;
+    if (__all_sync(0xffffffffu, ok && mbar_wait(&bars->s_full[0], 1, g, SITE_DIAG_MMA))) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(lane_addr + 128 + 32 * c, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o_out[row * D + 32 * c + i] = __uint_as_float(ov[i]);
+        }
+    }
+    if (threadIdx.x == 0) {
+        mma_commit(&bars->drain);
+        wait_quiet(&bars->drain, 0, kDrainLimitNs);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+__global__ void diag_wait_timeout_kernel(unsigned* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitGuard g{status, &abort_flag, limit_ns};
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, g, SITE_DIAG_TIMEOUT);  // nobody arrives
+    __syncthreads();
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillMaps& maps, const PrefillParams& prm, int grid,
+                             cudaStream_t stream) {
+    using C = Cfg<D>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_bf16_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    prefill_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(maps.q, maps.k, maps.v, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_block_rows() { return kItemRows; }
+int prefill_box_rows() { return BM; }
+
+cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse,
+                                const Shape& s, const LaunchEnv& env, int* grid_out,
+                                int* items_out, int* kernels_launched) {
+    PrefillParams prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.Hq = s.Hq;
+    prm.Hkv = s.Hkv;
+    prm.Tq = s.Tq;
+    prm.Tk = s.Tk;
+    prm.group = s.Hq / s.Hkv;
+    prm.causal = s.causal;
+    prm.scale_log2 = s.scale * 1.4426950408889634f;
+    prm.n_qblocks = (s.Tq + kItemRows - 1) / kItemRows;
+    prm.n_bh = s.B * s.Hq;
+    const long long items = static_cast<long long>(prm.n_qblocks) * prm.n_bh;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    prm.n_items = static_cast<int>(items);
+    prm.status = env.status;
+    prm.limit_ns = env.wait_limit_ns;
+    const int grid = static_cast<int>(items < env.num_sms ? items : env.num_sms);
+    if (grid_out) *grid_out = grid;
+    if (items_out) *items_out = prm.n_items;
+    if (kernels_launched) *kernels_launched = 1;
+    return (s.D == 64) ? launch_prefill_d<64>(maps, prm, grid, env.stream)
+                       : launch_prefill_d<128>(maps, prm, grid, env.stream);
+}
+
+cudaError_t launch_diag_mma_tile(const CUtensorMap& a, const CUtensorMap& b,
+                                 const CUtensorMap& v, float* s_out, float* o_out, int D,
+                                 const LaunchEnv& env) {
+    if (D == 64) {
+        constexpr int smem = 3 * Cfg<64>::kTileBytes + 256 + 1024;
+        cudaError_t e = cudaFuncSetAttribute(diag_mma_tile_kernel<64>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        diag_mma_tile_kernel<64><<<1, 128, smem, env.stream>>>(a, b, v, s_out, o_out, env.status,
+                                                                env.wait_limit_ns);
+    } else {
+        constexpr int smem = 3 * Cfg<128>::kTileBytes + 256 + 1024;
+        cudaError_t e = cudaFuncSetAttribute(diag_mma_tile_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        diag_mma_tile_kernel<128><<<1, 128, smem, env.stream>>>(a, b, v, s_out, o_out, env.status,
+                                                                 env.wait_limit_ns);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_diag_wait_timeout(const LaunchEnv& env, uint64_t limit_ns) {
+    diag_wait_timeout_kernel<<<1, 32, 0, env.stream>>>(env.status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace attn
