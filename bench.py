@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--no-secondary", action="store_true",
                     help="time only the primary workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None, metavar="WORKLOAD",
+                    help="only run --warmup + --steps calls of this named workload "
+                         "(no L2 flush, clocks, e2e or baselines): the command ncu captures")
     return ap.parse_args()
 
 
@@ -414,8 +417,32 @@ def run_reference(args):
     }
 
 
+def run_profile_case(args):
+    import torch
+    from transformer_attention_fwd_gb300 import build as b
+    b.build()
+    from transformer_attention_fwd_gb300 import attn
+    from transformer_attention_fwd_gb300.inputs import WORKLOADS, make_workload
+    w = WORKLOADS[args.profile_case]
+    q, k, v = (x.cuda() for x in make_workload(w, 0))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device="cuda")
+    fn = lambda: attn.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)  # noqa: E731
+    times = time_steps(fn, args.steps, args.warmup)
+    st = attn.device_status()
+    if st != attn.ATTN_OK:
+        raise RuntimeError(attn.last_error())
+    ms = sum(times) / len(times)
+    print(json.dumps({"profile_case": w.name, "ms_per_step": round(ms, 5),
+                      "tflops": round(w.flops / (ms * 1e-3) / 1e12, 3),
+                      "gbs": round(w.io_bytes() / (ms * 1e-3) / 1e9, 1)}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

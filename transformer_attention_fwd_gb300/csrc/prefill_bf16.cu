@@ -386,22 +386,26 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
             float sum = 0.0f;
-            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.
+            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.  The row
+            // sum adds the bf16-rounded weights, i.e. exactly the values the
+            // P.V product multiplies, so the weights applied to V sum to 1.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i]), p.scale_log2, neg_m));
                     const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i + 1]), p.scale_log2, neg_m));
-                    sum += a + b;
-                    r[2 * h][i] = pack_bf16x2(a, b);
+                    const uint32_t pk = pack_bf16x2(a, b);
+                    sum += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
+                    r[2 * h][i] = pk;
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i]), p.scale_log2, neg_m));
                     const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i + 1]), p.scale_log2, neg_m));
-                    sum += a + b;
-                    r[2 * h][16 + i] = pack_bf16x2(a, b);
+                    const uint32_t pk = pack_bf16x2(a, b);
+                    sum += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
+                    r[2 * h][16 + i] = pk;
                 }
             }
             tmem_st32(lane_addr + colS, r[0]);

@@ -63,6 +63,9 @@ WORKLOADS = {
         Workload("llama3_8b_prefill_bf16_b1_hq32_hkv8_t8192_d128_causal", 1, 32, 8, 8192, 8192, 128, True, "bf16"),
     "llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_noncausal":
         Workload("llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_noncausal", 1, 32, 8, 4096, 4096, 128, False, "bf16"),
+    # Half-length causal variant, used for small ncu captures of the prefill kernel.
+    "llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_causal":
+        Workload("llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_causal", 1, 32, 8, 4096, 4096, 128, True, "bf16"),
     "gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128":
         Workload("gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128", 64, 32, 8, 1, 4096, 128, False, "bf16"),
 }
