@@ -336,7 +336,7 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
         // Last visible key of this row and of the tile's first row.
         const int lim = p.causal ? min(row + off, p.Tk - 1) : p.Tk - 1;
         const int lim_first = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
-        float m = -INFINITY, l = 0.0f;
+        float m = -INFINITY, l = 0.0f, lr = 0.0f;
 
         for (int j = 0; j < n; ++j) {
             // Warp-uniform outcome: tcgen05.ld below needs the whole warp.
@@ -370,6 +370,7 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                 const float m_use = (m_new == -INFINITY) ? m : m_new;
                 const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_use);
                 l *= alpha;
+                lr *= alpha;
                 if (j > 0) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
@@ -385,10 +386,11 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                 m = m_use;
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            float sum = 0.0f;
-            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.  The row
-            // sum adds the bf16-rounded weights, i.e. exactly the values the
-            // P.V product multiplies, so the weights applied to V sum to 1.
+            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.  Two row
+            // sums: l (exact weights) gives the log-sum-exp; lr adds the
+            // bf16-rounded weights, i.e. exactly the values the P.V product
+            // multiplies, and normalises O so its weights sum to 1.
+            float sum = 0.0f, sum_r = 0.0f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -396,7 +398,8 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                     const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i]), p.scale_log2, neg_m));
                     const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i + 1]), p.scale_log2, neg_m));
                     const uint32_t pk = pack_bf16x2(a, b);
-                    sum += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
+                    sum += a + b;
+                    sum_r += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
                     r[2 * h][i] = pk;
                 }
 #pragma unroll
@@ -404,7 +407,8 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                     const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i]), p.scale_log2, neg_m));
                     const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i + 1]), p.scale_log2, neg_m));
                     const uint32_t pk = pack_bf16x2(a, b);
-                    sum += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
+                    sum += a + b;
+                    sum_r += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
                     r[2 * h][16 + i] = pk;
                 }
             }
@@ -412,6 +416,7 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
             tmem_st32(lane_addr + colS + 32, r[2]);
             tmem_wait_st();
             l += sum;
+            lr += sum_r;
             tc_fence_before_sync();
             mbar_arrive(&bars->p_full[t]);
         }
@@ -421,7 +426,7 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
             return;
         ++o_cnt;
         tc_fence_after_sync();
-        const float inv_l = 1.0f / l;
+        const float inv_l = 1.0f / lr;
         const bool in_range = row < p.Tq;
         uint16_t* orow = p.o + (static_cast<int64_t>(it.bh) * p.Tq + row) * D;
 #pragma unroll
