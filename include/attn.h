@@ -104,6 +104,42 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
                             cudaStream_t stream);
 
 /*
+ * attn_fwd_decode_noalloc -- attn_fwd_decode that allocates no device memory.
+ * The pages have no counterpart to this entry point: it is an interface
+ * variant of the decode call, not part of the method.
+ *
+ * Some callers cannot let a library allocate device memory during a call:
+ * serving engines and frameworks that reserve all of HBM for their own
+ * allocator up front (a driver allocation in the middle of a decode step could
+ * then fail with out-of-memory), or that keep allocation, and the
+ * synchronisation it may bring, out of a latency-critical decode step.  This
+ * call computes exactly what attn_fwd_decode computes, with the same
+ * arguments and errors, but writes the split partials into a fixed workspace
+ * that is part of the library's device image: an 8 MiB array that every GPU
+ * loading libattn.so holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Size limit: the partials take B*Hq*splits*(D+1)*4 bytes and must fit in the
+ * 8 MiB.  With num_splits = 0 the automatic split count is lowered until they
+ * fit (one split needs no workspace at all); an explicit num_splits that does
+ * not fit returns ATTN_ERR_UNSUPPORTED with the sizes in attn_last_error().
+ *
+ * Sharing: every call uses the same array and overwrites the part it reads
+ * before reading it, so nothing has to start at zero; but calls whose kernels
+ * can run at the same time on the GPU (e.g. on two streams with no ordering
+ * between them) race on the array and give undefined results.  Order such
+ * calls, e.g. issue them on one stream.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * once (cudaGetSymbolAddress, with that device current).  Make that first call
+ * before any stream capture.
+ */
+attn_status attn_fwd_decode_noalloc(const void* q, const void* k, const void* v,
+                                    void* o, float* lse, int B, int Hq, int Hkv,
+                                    int Tk, int D, float scale, int num_splits,
+                                    cudaStream_t stream);
+
+/*
  * attn_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns ATTN_ERR_TIMEOUT when a
  * kernel gave up on a pipeline wait since the last call (its outputs are

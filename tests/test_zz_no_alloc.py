@@ -1,0 +1,77 @@
+"""attn_fwd_decode_noalloc: the decode entry point that allocates nothing.
+
+It exists for callers that cannot let a library allocate device memory in the
+middle of a call (engines that reserve all of HBM for their own allocator, or
+that keep allocation out of a latency-critical decode step).  Its partial
+results live in a fixed 8 MiB workspace inside the library instead of memory
+allocated per call.  Here it is called straight through the C ABI, twice in a
+row with different shapes, and each result is checked against the allocating
+entry point attn_fwd_decode within the parity tolerances the other decode
+tests use.  This file sorts last so that a run stopping at its first failure
+has already run every other test.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, to_dev
+from transformer_attention_fwd_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 8 << 20
+
+
+def _noalloc():
+    a = attn()
+    fn = ctypes.CDLL(a.LIB_PATH).attn_fwd_decode_noalloc
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, P]
+    fn.restype = ctypes.c_int
+    return a, fn
+
+
+def _call(fn, q, k, v, splits):
+    B, Hq, _, D = q.shape
+    _, Hkv, Tk, _ = k.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device="cuda")
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, Hq, Hkv,
+            Tk, D, D ** -0.5, splits, torch.cuda.current_stream().cuda_stream)
+    return st, o, lse
+
+
+def test_noalloc_decode_matches_allocating_decode_on_two_calls():
+    a, fn = _noalloc()
+    cases = [(16, 32, 8, 4096, 128, 0), (4, 12, 4, 3001, 64, 5)]
+    outs = []
+    for i, (B, Hq, Hkv, Tk, D, splits) in enumerate(cases):
+        q, k, v = to_dev(*make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=20 + i))
+        st, o, lse = _call(fn, q, k, v, splits)
+        assert st == a.ATTN_OK, a.last_error()
+        outs.append((q, k, v, splits, o, lse))
+    torch.cuda.synchronize()
+    check_status(a)
+    for q, k, v, splits, o, lse in outs:
+        o_ref, lse_ref = a.attn_fwd_decode(q, k, v, num_splits=splits)
+        check_status(a)
+        assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
+        assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16
+
+
+def test_noalloc_rejects_partials_beyond_the_static_workspace():
+    a, fn = _noalloc()
+    B, Hq, Hkv, Tk, D = 64, 32, 8, 4096, 128
+    q, k, v = to_dev(*make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=30))
+    splits = 16  # 64*32*16*129*4 bytes > 8 MiB
+    assert B * Hq * splits * (D + 1) * 4 > SCRATCH_BYTES
+    st, _, _ = _call(fn, q, k, v, splits)
+    assert st == a.ATTN_ERR_UNSUPPORTED
+    assert "static workspace" in a.last_error()
+    st, o, lse = _call(fn, q, k, v, 0)  # automatic count is capped to fit
+    assert st == a.ATTN_OK, a.last_error()
+    o_ref, lse_ref = a.attn_fwd_decode(q, k, v)
+    check_status(a)
+    assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
+    assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16

@@ -385,3 +385,91 @@ attn_status attn_diag_wait_timeout(long long timeout_ns, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode (attn_fwd_decode_noalloc).
+// ---------------------------------------------------------------------------
+namespace attn {
+namespace {
+
+// Workspace of attn_fwd_decode_noalloc: a fixed array in the library's device
+// image instead of memory allocated per call.  Every GPU that loads the
+// library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The host-side
+// name of the array is only a stand-in, never a device address, so the
+// address is looked up once per device (the first call on that device) with
+// that device current.
+attn_status noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return ATTN_OK;
+}
+
+size_t noalloc_bytes(const Shape& s, int splits) {
+    if (splits <= 1) return 0;
+    return static_cast<size_t>(s.B) * s.Hq * splits * (s.D + 1) * sizeof(float);
+}
+
+int nonempty_splits(int splits, int Tk) {
+    if (splits > 256) splits = 256;
+    if (splits > Tk) splits = Tk;
+    if (splits < 1) splits = 1;
+    const int per = (Tk + splits - 1) / splits;
+    return (Tk + per - 1) / per;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" attn_status attn_fwd_decode_noalloc(const void* q, const void* k, const void* v,
+                                               void* o, float* lse, int B, int Hq, int Hkv,
+                                               int Tk, int D, float scale, int num_splits,
+                                               cudaStream_t stream) {
+    using namespace attn;
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, 1, Tk, D, 0, scale);
+    if (st != ATTN_OK) return st;
+    if (num_splits < 0 || num_splits > 256)
+        return fail(ATTN_ERR_INVALID_ARG, "num_splits must be in 0..256 (got %d)", num_splits);
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    const Shape s{B, Hq, Hkv, 1, Tk, D, 0, scale};
+    int splits = nonempty_splits(num_splits > 0 ? num_splits : decode_choose_splits(s, env.num_sms), Tk);
+    if (num_splits == 0)  // automatic count: lower it until the partials fit
+        while (splits > 1 && noalloc_bytes(s, splits) > kNoAllocScratchBytes)
+            splits = nonempty_splits(splits - 1, Tk);
+    if (noalloc_bytes(s, splits) > kNoAllocScratchBytes)
+        return fail(ATTN_ERR_UNSUPPORTED,
+                    "decode with %d splits needs %zu bytes of scratch; the static workspace holds "
+                    "%zu bytes (B*Hq*splits*(D+1)*4 must fit; pass fewer splits)",
+                    splits, noalloc_bytes(s, splits), kNoAllocScratchBytes);
+    float* ws_o = nullptr;
+    float* ws_lse = nullptr;
+    if (splits > 1) {
+        void* ws = nullptr;
+        st = noalloc_scratch(env.device, &ws);
+        if (st != ATTN_OK) return st;
+        ws_o = static_cast<float*>(ws);
+        ws_lse = ws_o + static_cast<size_t>(B) * Hq * splits * D;
+    }
+    int kernels = 0;
+    cudaError_t e = launch_decode_bf16(static_cast<const uint16_t*>(q),
+                                       static_cast<const uint16_t*>(k),
+                                       static_cast<const uint16_t*>(v), static_cast<uint16_t*>(o),
+                                       lse, ws_o, ws_lse, s, splits, env, &kernels);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    record_launch(B * Hkv, splits, kernels);
+    return ok();
+}
