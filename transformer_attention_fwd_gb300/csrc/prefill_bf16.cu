@@ -58,10 +58,11 @@ template <int D>
 struct Cfg {
     static constexpr int kChunks = D / kBoxCols;
     static constexpr int kTileBytes = kChunks * kBoxBytes;  // 128 rows x D bf16
+    static constexpr int kQStages = (D == 128) ? 1 : 2;    // Q buffers (2 query tiles each)
     static constexpr int kKStages = (D == 128) ? 3 : 4;
     static constexpr int kVStages = (D == 128) ? 2 : 4;
     static constexpr int kQOff = 0;
-    static constexpr int kKOff = kQOff + NQT * kTileBytes;
+    static constexpr int kKOff = kQOff + kQStages * NQT * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
     static constexpr int kBarBytes = 256;
@@ -71,8 +72,20 @@ struct Cfg {
     __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
 };
 
+// Register split (setmaxnreg): the CTA launches with 168 registers per thread
+// (384 x 168 = 64512); the four control warps drop to 64 and the eight
+// softmax warps rise to 216: 128 x 64 + 256 x 216 = 63488 <= 64512.
+constexpr int kCtrlRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * 168, "register split too large");
+
+// Fraction of the exponentials of an unmasked tile evaluated by the
+// polynomial (exp2_poly_x2) instead of the MUFU unit: pairs with
+// (i % kPolyEvery) == kPolyEvery - 1, i.e. one pair in kPolyEvery.
+constexpr int kPolyEvery = 4;
+
 struct Bars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[4], k_empty[4];
     uint64_t v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
@@ -97,7 +110,7 @@ struct Item {
     int n[2];  // key tiles visited by query tile 0 / 1 (0: tile is past Tq)
 };
 
-// Work item idx -> (bh, query block).  Query blocks are handed out from the
+// Work item idx -> (bh, query block).  Query blocks are numbered from the
 // last (longest under the causal mask) to the first.
 __device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p) {
     Item it;
@@ -120,6 +133,16 @@ __device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p) {
         }
     }
     return it;
+}
+
+// The k-th item of this CTA: the longest-first list is dealt in passes of
+// gridDim.x items, alternating direction (snake order), which balances the
+// causal work across CTAs without any global counter.  -1 when this CTA has
+// no item in the (last, partial) pass k.
+__device__ __forceinline__ int snake_item(int k, int n_items) {
+    const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const int idx = k * g + ((k & 1) ? (g - 1 - c) : c);
+    return idx < n_items ? idx : -1;
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -171,23 +194,28 @@ __device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint
                             Bars* bars, const PrefillParams& p, const WaitGuard& g) {
     using C = Cfg<D>;
     uint32_t kv_it = 0, q_it = 0;
-    int issued_q = 0;
-    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
+        const int idx = snake_item(k, p.n_items);
+        if (idx < 0) continue;
         const Item it = decode_item(idx, p);
         const int nkv = max(it.n[0], it.n[1]);
-        if (q_it > 0 && !mbar_wait(&bars->q_empty, (q_it - 1) & 1, g, SITE_Q_EMPTY)) goto drain;
-        mbar_arrive_expect_tx(&bars->q_full,
+        const int qs = q_it % C::kQStages;
+        const uint32_t qph = (q_it / C::kQStages) & 1;
+        if (q_it >= (uint32_t)C::kQStages &&
+            !mbar_wait(&bars->q_empty[qs], qph ^ 1, g, SITE_Q_EMPTY))
+            goto drain;
+        mbar_arrive_expect_tx(&bars->q_full[qs],
                               ((it.n[0] > 0) + (it.n[1] > 0)) * C::kTileBytes);
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (it.n[t] == 0) continue;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes, tmQ,
-                            &bars->q_full, c * kBoxCols, it.qb * kItemRows + t * BM, it.bh);
+                tma_load_3d(smem + C::kQOff + (qs * NQT + t) * C::kTileBytes + c * kBoxBytes,
+                            tmQ, &bars->q_full[qs], c * kBoxCols, it.qb * kItemRows + t * BM,
+                            it.bh);
         }
         ++q_it;
-        issued_q = 1;
         for (int j = 0; j < nkv; ++j, ++kv_it) {
             const int s = kv_it % C::kKStages;
             const uint32_t ph = (kv_it / C::kKStages) & 1;
@@ -203,7 +231,8 @@ __device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint
     return;
 drain:
     // Let copies already in flight land before the CTA leaves.
-    if (issued_q) wait_quiet(&bars->q_full, (q_it - 1) & 1, kDrainLimitNs);
+    for (uint32_t i = (q_it > (uint32_t)C::kQStages ? q_it - C::kQStages : 0); i < q_it; ++i)
+        wait_quiet(&bars->q_full[i % C::kQStages], (i / C::kQStages) & 1, kDrainLimitNs);
     for (uint32_t i = (kv_it > (uint32_t)C::kKStages ? kv_it - C::kKStages : 0); i < kv_it; ++i)
         wait_quiet(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, kDrainLimitNs);
 }
@@ -213,7 +242,9 @@ __device__ void producer_v(const CUtensorMap* tmV, uint8_t* smem, Bars* bars,
                            const PrefillParams& p, const WaitGuard& g) {
     using C = Cfg<D>;
     uint32_t kv_it = 0;
-    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
+        const int idx = snake_item(k, p.n_items);
+        if (idx < 0) continue;
         const Item it = decode_item(idx, p);
         const int nkv = max(it.n[0], it.n[1]);
         for (int j = 0; j < nkv; ++j, ++kv_it) {
@@ -238,19 +269,22 @@ template <int D>
 __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const PrefillParams& p,
                            const WaitGuard& g) {
     using C = Cfg<D>;
-    const uint32_t q_base = smem_u32(smem + C::kQOff);
     const uint32_t k_base = smem_u32(smem + C::kKOff);
     const uint32_t v_base = smem_u32(smem + C::kVOff);
     uint32_t kv_it = 0, q_it = 0;
     uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
 
-    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
+        const int idx = snake_item(k, p.n_items);
+        if (idx < 0) continue;
         const Item it = decode_item(idx, p);
         const int n0 = it.n[0], n1 = it.n[1];
         const int nkv = max(n0, n1);
-        if (!mbar_wait(&bars->q_full, q_it & 1, g, SITE_Q_FULL)) goto drain;
+        const int qs = q_it % C::kQStages;
+        if (!mbar_wait(&bars->q_full[qs], (q_it / C::kQStages) & 1, g, SITE_Q_FULL)) goto drain;
         ++q_it;
         tc_fence_after_sync();
+        const uint32_t q_base = smem_u32(smem + C::kQOff + qs * NQT * C::kTileBytes);
         const uint32_t first = kv_it;
         for (int j = 0; j <= nkv; ++j) {
             const uint32_t itj = first + j;
@@ -291,7 +325,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                     mma_commit(&bars->s_full[1]);
                 }
                 mma_commit(&bars->k_empty[ks]);
-                if (j == nkv - 1) mma_commit(&bars->q_empty);
+                if (j == nkv - 1) mma_commit(&bars->q_empty[qs]);
                 if (j < n0) {  // PV0(j)
                     if (!mbar_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
                     ++p_cnt[0];
@@ -316,6 +350,45 @@ drain:
     wait_quiet(&bars->drain, 0, kDrainLimitNs);
 }
 
+// Exponentials of one row of a tile, packed to bf16 pairs in place:
+// r[c][0..15] receives the 16 packed pairs of chunk c (keys 32c .. 32c+31).
+// Returns the exact and the bf16-rounded row sums as packed pairs.
+template <bool kPoly>
+__device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2, float neg_m,
+                                         float& sum_exact, float& sum_rounded) {
+    const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+    const uint64_t nm2 = f2_pack(neg_m, neg_m);
+    uint64_t acc_e[2] = {0, 0}, acc_r[2] = {0, 0};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[c][2 * i]),
+                                               __uint_as_float(r[c][2 * i + 1])), sc2, nm2);
+            float a, b;
+            if (kPoly && (i % kPolyEvery) == kPolyEvery - 1) {
+                exp2_poly_x2(x2, a, b);
+            } else {
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                a = ex2_approx(x0);
+                b = ex2_approx(x1);
+            }
+            const uint32_t pk = pack_bf16x2(a, b);
+            acc_e[i & 1] = f2_add(acc_e[i & 1], f2_pack(a, b));
+            acc_r[i & 1] = f2_add(acc_r[i & 1], f2_pack(bf16_lo_to_f32(pk), bf16_hi_to_f32(pk)));
+            r[c][i] = pk;
+        }
+    }
+    float e0, e1, e2, e3, r0, r1, r2, r3;
+    f2_unpack(acc_e[0], e0, e1);
+    f2_unpack(acc_e[1], e2, e3);
+    f2_unpack(acc_r[0], r0, r1);
+    f2_unpack(acc_r[1], r2, r3);
+    sum_exact = (e0 + e1) + (e2 + e3);
+    sum_rounded = (r0 + r1) + (r2 + r3);
+}
+
 template <int D>
 __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams& p,
                            const WaitGuard& g) {
@@ -327,7 +400,9 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
     const int off = p.Tk - p.Tq;
     uint32_t s_cnt = 0, o_cnt = 0;
 
-    for (int idx = blockIdx.x; idx < p.n_items; idx += gridDim.x) {
+    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
+        const int idx = snake_item(k, p.n_items);
+        if (idx < 0) continue;
         const Item it = decode_item(idx, p);
         const int n = it.n[t];
         if (n == 0) continue;
@@ -352,18 +427,25 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
             reg_order(r[2]);
             reg_order(r[3]);
             const int kbase = j * BN;
-            if (kbase + BN - 1 > lim_first) {  // tile straddles the diagonal or Tk
+            const bool masked = kbase + BN - 1 > lim_first;  // straddles the diagonal or Tk
+            if (masked) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (kbase + 32 * c + i > lim) r[c][i] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // Row maximum of the raw scores: four independent 3-input max chains.
+            float mc[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                float a = fmaxf(__uint_as_float(r[c][0]), __uint_as_float(r[c][1]));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r[c][i]));
+                for (int i = 2; i < 32; i += 2)
+                    a = fmax3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+                mc[c] = a;
+            }
+            const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
             const float m_new = fmaxf(m, mx * p.scale_log2);
             const bool need = m_new > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
@@ -386,42 +468,32 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                 m = m_use;
             }
             const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            // P = 2^(s*scale*log2e - m) as packed bf16 pairs, in place.  Two row
-            // sums: l (exact weights) gives the log-sum-exp; lr adds the
-            // bf16-rounded weights, i.e. exactly the values the P.V product
-            // multiplies, and normalises O so its weights sum to 1.
-            float sum = 0.0f, sum_r = 0.0f;
+            // P = 2^(s*scale*log2e - m) as packed bf16 pairs.  Two row sums:
+            // l (exact weights) gives the log-sum-exp; lr adds the bf16-rounded
+            // weights, i.e. exactly the values the P.V product multiplies, and
+            // normalises O so its weights sum to 1.  Masked tiles use the MUFU
+            // exponential only, so masked weights are exactly 0.
+            float sum_e, sum_r;
+            if (masked)
+                row_exp2<false>(r, p.scale_log2, neg_m, sum_e, sum_r);
+            else
+                row_exp2<true>(r, p.scale_log2, neg_m, sum_e, sum_r);
+            // Gather the 64 packed columns: chunks 0,1 -> r[0], chunks 2,3 -> r[2].
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i]), p.scale_log2, neg_m));
-                    const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h][2 * i + 1]), p.scale_log2, neg_m));
-                    const uint32_t pk = pack_bf16x2(a, b);
-                    sum += a + b;
-                    sum_r += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
-                    r[2 * h][i] = pk;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i]), p.scale_log2, neg_m));
-                    const float b = ex2_approx(fmaf(__uint_as_float(r[2 * h + 1][2 * i + 1]), p.scale_log2, neg_m));
-                    const uint32_t pk = pack_bf16x2(a, b);
-                    sum += a + b;
-                    sum_r += bf16_lo_to_f32(pk) + bf16_hi_to_f32(pk);
-                    r[2 * h][16 + i] = pk;
-                }
+            for (int i = 0; i < 16; ++i) {
+                r[0][16 + i] = r[1][i];
+                r[2][16 + i] = r[3][i];
             }
             tmem_st32(lane_addr + colS, r[0]);
             tmem_st32(lane_addr + colS + 32, r[2]);
             tmem_wait_st();
-            l += sum;
+            l += sum_e;
             lr += sum_r;
             tc_fence_before_sync();
             mbar_arrive(&bars->p_full[t]);
         }
 
-        // Epilogue: O = O_acc / l -> bf16; lse = (m + log2 l) * ln 2.
+        // Epilogue: O = O_acc / lr -> bf16; lse = (m + log2 l) * ln 2.
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], o_cnt & 1, g, SITE_O_FULL)))
             return;
         ++o_cnt;
@@ -465,8 +537,10 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->q_empty[s], 1);
+        }
         for (int s = 0; s < 4; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
@@ -498,13 +572,17 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t tmem = bars->tmem_base;
     const WaitGuard g{p.status, &bars->abort, p.limit_ns};
 
-    if (warp == 0) {
-        if (lane == 0) producer_qk<D>(&tmQ, &tmK, smem, bars, p, g);
-    } else if (warp == 3) {
-        if (lane == 0) producer_v<D>(&tmV, smem, bars, p, g);
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer<D>(smem, bars, tmem, p, g);
-    } else if (warp >= 4) {
+    if (warp < 4) {
+        regs_decrease<kCtrlRegs>();
+        if (warp == 0) {
+            if (lane == 0) producer_qk<D>(&tmQ, &tmK, smem, bars, p, g);
+        } else if (warp == 3) {
+            if (lane == 0) producer_v<D>(&tmV, smem, bars, p, g);
+        } else if (warp == 1) {
+            if (lane == 0) mma_issuer<D>(smem, bars, tmem, p, g);
+        }
+    } else {
+        regs_increase<kSoftmaxRegs>();
         softmax_wg<D>((warp - 4) / 4, bars, tmem, p, g);
     }
 
@@ -536,7 +614,7 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     const int row = threadIdx.x;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_full[0], 1);
         mbar_init(&bars->s_full[0], 1);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -555,13 +633,13 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     bool ok = true;
 
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bars->q_full, 3 * C::kTileBytes);
+        mbar_arrive_expect_tx(&bars->q_full[0], 3 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_2d(sa + c * kBoxBytes, &tmA, &bars->q_full, c * kBoxCols, 0);
-            tma_load_2d(sb + c * kBoxBytes, &tmB, &bars->q_full, c * kBoxCols, 0);
-            tma_load_2d(sv + c * kBoxBytes, &tmV, &bars->q_full, c * kBoxCols, 0);
+            tma_load_2d(sa + c * kBoxBytes, &tmA, &bars->q_full[0], c * kBoxCols, 0);
+            tma_load_2d(sb + c * kBoxBytes, &tmB, &bars->q_full[0], c * kBoxCols, 0);
+            tma_load_2d(sv + c * kBoxBytes, &tmV, &bars->q_full[0], c * kBoxCols, 0);
         }
-        if (mbar_wait(&bars->q_full, 0, g, SITE_DIAG_LOAD)) {
+        if (mbar_wait(&bars->q_full[0], 0, g, SITE_DIAG_LOAD)) {
             tc_fence_after_sync();
             issue_qk<D>(tmem, smem_u32(sa), smem_u32(sb));
             mma_commit(&bars->s_full[0]);

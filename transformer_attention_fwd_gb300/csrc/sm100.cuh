@@ -276,6 +276,43 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs (one 64-bit register pair) and the sm_100 f32x2 ops that
+// do two fp32 operations per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Per-warp register budget change (values are multiples of 8); every thread
+// of the warp executes it.
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -287,6 +324,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// 2^x on the FMA and integer pipes, for x <= 64 (arguments below -126 give
+// 2^-126 instead of 0).  Cody-Waite split x = j + f with j = rint(x) (the
+// 1.5 * 2^23 rounding trick, exact in fp32 for |x| < 2^22) and
+// f in [-1/2, 1/2]; 2^f by a degree-4 polynomial whose maximum relative error
+// on [-1/2, 1/2] is minimised (Remez exchange; csrc/fit_exp2_poly.py prints
+// the coefficients and the bound, 2.7e-6); 2^j is added to the exponent field.
+// Two arguments at a time through the packed f32x2 instructions.
+__device__ __forceinline__ void exp2_poly_x2(uint64_t x2, float& y0, float& y1) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    float x0, x1;
+    f2_unpack(x2, x0, x1);
+    const uint64_t xc = f2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+    const uint64_t t = f2_add(xc, f2_pack(kMagic, kMagic));
+    const uint64_t j = f2_add(t, f2_pack(-kMagic, -kMagic));
+    const uint64_t f = f2_fma(j, f2_pack(-1.0f, -1.0f), xc);
+    uint64_t p = f2_fma(f2_pack(0.009570102207362652f, 0.009570102207362652f), f,
+                        f2_pack(0.05591785907745361f, 0.05591785907745361f));
+    p = f2_fma(p, f, f2_pack(0.240247443318367f, 0.240247443318367f));
+    p = f2_fma(p, f, f2_pack(0.6931217908859253f, 0.6931217908859253f));
+    p = f2_fma(p, f, f2_pack(0.9999992847442627f, 0.9999992847442627f));
+    float p0, p1, t0, t1;
+    f2_unpack(p, p0, p1);
+    f2_unpack(t, t0, t1);
+    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
