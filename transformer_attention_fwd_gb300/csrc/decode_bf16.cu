@@ -370,19 +370,49 @@ int heads_per_cta(int group) {
     return 1;
 }
 
+// Resident CTAs per SM of the split kernel used for this shape.
+int split_kernel_occupancy(int D, int hc) {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+#define ATTN_OCC(DD, HH) \
+    if (D == DD && hc == HH) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<DD, HH>, kThreads, 0);
+    ATTN_OCC(64, 1) ATTN_OCC(64, 2) ATTN_OCC(64, 4) ATTN_OCC(64, 8)
+    ATTN_OCC(128, 1) ATTN_OCC(128, 2) ATTN_OCC(128, 4) ATTN_OCC(128, 8)
+#undef ATTN_OCC
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return n > 0 ? n : 1;
+}
+
 }  // namespace
 
+// Split count: maximise the fill of the last wave of CTAs (waves / ceil(waves)
+// over the SM slots the kernel can occupy), minus a small charge per split for
+// the partial results each split writes and the combine reads; at least 256
+// keys per split.
 int decode_choose_splits(const Shape& s, int num_sms) {
     const int group = s.Hq / s.Hkv;
-    const int chunks = group / heads_per_cta(group);
-    const long long ctas = static_cast<long long>(s.B) * s.Hkv * chunks;
-    // Aim for about 8 CTAs per SM, but keep at least 256 keys per split.
-    long long want = (8LL * num_sms + ctas - 1) / ctas;
-    const long long max_by_keys = (s.Tk + 255) / 256;
-    if (want > max_by_keys) want = max_by_keys;
-    if (want > 256) want = 256;
-    if (want < 1) want = 1;
-    return static_cast<int>(want);
+    const int hc = heads_per_cta(group);
+    const int chunks = group / hc;
+    const double ctas = static_cast<double>(s.B) * s.Hkv * chunks;
+    const double slots = static_cast<double>(num_sms) * split_kernel_occupancy(s.D, hc);
+    int max_s = (s.Tk + 255) / 256;
+    if (max_s > 16) max_s = 16;
+    if (max_s < 1) max_s = 1;
+    int best = 1;
+    double best_score = -1.0;
+    for (int sp = 1; sp <= max_s; ++sp) {
+        const double waves = ctas * sp / slots;
+        const double fill = waves / std::ceil(waves);
+        const double score = fill - 0.01 * sp;
+        if (score > best_score + 1e-9) {
+            best_score = score;
+            best = sp;
+        }
+    }
+    return best;
 }
 
 size_t decode_workspace_bytes(const Shape& s, int splits) {

@@ -79,10 +79,17 @@ constexpr int kCtrlRegs = 64;
 constexpr int kSoftmaxRegs = 216;
 static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * 168, "register split too large");
 
-// Fraction of the exponentials of an unmasked tile evaluated by the
-// polynomial (exp2_poly_x2) instead of the MUFU unit: pairs with
-// (i % kPolyEvery) == kPolyEvery - 1, i.e. one pair in kPolyEvery.
-constexpr int kPolyEvery = 4;
+// Share of the exponentials of an unmasked tile evaluated by the polynomial
+// (exp2_poly_x2) instead of the MUFU unit: pairs with
+// (i % kPolyEvery) == kPolyEvery - 1, i.e. one pair in kPolyEvery (0: none).
+// GB300's MUFU issues ex2 at twice the rate of earlier Blackwell parts and the
+// softmax warps are bound by instruction issue, not by MUFU, so moving work
+// to the FMA pipe does not pay: measured on the T=8192 causal workload, none
+// (1150 TFLOP/s) beat one pair in 16 (1112), in 8 (1093) and in 4 (1057).
+#ifndef ATTN_PREFILL_POLY_EVERY
+#define ATTN_PREFILL_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = ATTN_PREFILL_POLY_EVERY;
 
 struct Bars {
     uint64_t q_full[2], q_empty[2];
@@ -358,7 +365,8 @@ __device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2,
                                          float& sum_exact, float& sum_rounded) {
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
     const uint64_t nm2 = f2_pack(neg_m, neg_m);
-    uint64_t acc_e[2] = {0, 0}, acc_r[2] = {0, 0};
+    uint64_t acc_e[2] = {0, 0};
+    float acc_r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -366,7 +374,7 @@ __device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2,
             const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[c][2 * i]),
                                                __uint_as_float(r[c][2 * i + 1])), sc2, nm2);
             float a, b;
-            if (kPoly && (i % kPolyEvery) == kPolyEvery - 1) {
+            if (kPoly && kPolyEvery > 0 && (i % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
                 exp2_poly_x2(x2, a, b);
             } else {
                 float x0, x1;
@@ -376,17 +384,15 @@ __device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2,
             }
             const uint32_t pk = pack_bf16x2(a, b);
             acc_e[i & 1] = f2_add(acc_e[i & 1], f2_pack(a, b));
-            acc_r[i & 1] = f2_add(acc_r[i & 1], f2_pack(bf16_lo_to_f32(pk), bf16_hi_to_f32(pk)));
+            add_bf16x2_to_f32(pk, acc_r[2 * (i & 1)], acc_r[2 * (i & 1) + 1]);
             r[c][i] = pk;
         }
     }
-    float e0, e1, e2, e3, r0, r1, r2, r3;
+    float e0, e1, e2, e3;
     f2_unpack(acc_e[0], e0, e1);
     f2_unpack(acc_e[1], e2, e3);
-    f2_unpack(acc_r[0], r0, r1);
-    f2_unpack(acc_r[1], r2, r3);
     sum_exact = (e0 + e1) + (e2 + e3);
-    sum_rounded = (r0 + r1) + (r2 + r3);
+    sum_rounded = (acc_r[0] + acc_r[1]) + (acc_r[2] + acc_r[3]);
 }
 
 template <int D>
@@ -478,14 +484,9 @@ __device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams
                 row_exp2<false>(r, p.scale_log2, neg_m, sum_e, sum_r);
             else
                 row_exp2<true>(r, p.scale_log2, neg_m, sum_e, sum_r);
-            // Gather the 64 packed columns: chunks 0,1 -> r[0], chunks 2,3 -> r[2].
+            // Chunk c's 16 packed columns hold keys 32c .. 32c+31.
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                r[0][16 + i] = r[1][i];
-                r[2][16 + i] = r[3][i];
-            }
-            tmem_st32(lane_addr + colS, r[0]);
-            tmem_st32(lane_addr + colS + 32, r[2]);
+            for (int c = 0; c < 4; ++c) tmem_st16(lane_addr + colS + 16 * c, r[c]);
             tmem_wait_st();
             l += sum_e;
             lr += sum_r;
