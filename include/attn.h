@@ -92,11 +92,14 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v,
  * num_splits contiguous ranges processed in parallel; each range yields a
  * normalised partial output and its log-sum-exp, merged afterwards with the
  * block-merge rule of "Self-Attention机制深入理解" §12.3.
- * num_splits: 0 = choose from B*Hkv and the SM count; otherwise 1..256
- * (clamped to the number of keys).  The result does not depend on the split
- * count beyond float32 rounding.  Partial results live in a workspace the
- * library allocates and frees on `stream` (stream-ordered); a failed
- * allocation returns ATTN_ERR_NO_MEMORY.
+ * num_splits: 0 = automatic: all keys of all (b, hkv) are laid end to end
+ * and cut into one equal slice per SM, each slice streamed by one persistent
+ * CTA (a (b, hkv) cut by a slice boundary is merged the same way).
+ * 1..256 = that many equal ranges per (b, hkv) (clamped to the number of
+ * keys).  The result does not depend on the split choice beyond float32
+ * rounding.  Partial results live in a workspace the library allocates and
+ * frees on `stream` (stream-ordered); a failed allocation returns
+ * ATTN_ERR_NO_MEMORY.
  */
 attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
                             void* o, float* lse, int B, int Hq, int Hkv,

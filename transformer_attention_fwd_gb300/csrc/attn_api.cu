@@ -227,9 +227,33 @@ attn_status run_prefill(const void* q, const void* k, const void* v, void* o, fl
     return ok();
 }
 
+// Automatic mode: the stream-K kernel (equal key slices per SM); its
+// workspace holds the fragments of the units that slice boundaries cut.
+attn_status run_decode_stream(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const Shape& s, const LaunchEnv& env) {
+    const size_t bytes = decode_stream_workspace_bytes(s, env.num_sms);
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
+    if (e != cudaSuccess || ws == nullptr) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, "decode workspace of %zu bytes: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    int grid = 0, kernels = 0;
+    e = launch_decode_stream_bf16(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+                                  static_cast<const uint16_t*>(v), static_cast<uint16_t*>(o), lse,
+                                  static_cast<float*>(ws), s, env, &grid, &kernels);
+    cudaError_t f = cudaFreeAsync(ws, env.stream);
+    if (e == cudaSuccess && f != cudaSuccess) e = f;
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    record_launch(grid, 0, kernels);
+    return ok();
+}
+
 attn_status run_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                        const Shape& s, int num_splits, const LaunchEnv& env) {
-    int splits = num_splits > 0 ? num_splits : decode_choose_splits(s, env.num_sms);
+    if (num_splits == 0) return run_decode_stream(q, k, v, o, lse, s, env);
+    int splits = num_splits;
     if (splits > 256) splits = 256;
     if (splits > s.Tk) splits = s.Tk;
     // Recompute so that no split is empty.

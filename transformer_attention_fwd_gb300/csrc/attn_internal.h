@@ -48,6 +48,13 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
                                const Shape& s, int splits, const LaunchEnv& env,
                                int* kernels_launched);
 int decode_choose_splits(const Shape& s, int num_sms);
+
+// Stream-K decode: one persistent CTA per SM over equal slices of all keys;
+// ws holds the fragments of units that slice boundaries cut.
+size_t decode_stream_workspace_bytes(const Shape& s, int num_sms);
+cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                      uint16_t* o, float* lse, float* ws, const Shape& s,
+                                      const LaunchEnv& env, int* grid_out, int* kernels_launched);
 size_t decode_workspace_bytes(const Shape& s, int splits);
 
 // Diagnostics.

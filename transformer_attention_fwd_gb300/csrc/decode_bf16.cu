@@ -452,4 +452,456 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
     return e;
 }
 
+// ---------------------------------------------------------------------------
+// Stream-K decode (automatic mode).
+//
+// One persistent CTA per SM.  The keys of all (b, hkv, head chunk) units are
+// laid end to end and cut into one equal contiguous slice per CTA, so every
+// CTA streams the same number of bytes whatever B, Hkv and Tk are.  A slice
+// covers whole units and at most two unit fragments; a unit cut by slice
+// boundaries is merged by the combine kernel (block-merge rule,
+// "Self-Attention机制深入理解" §12.3).  A producer warp copies each chunk of K
+// and V rows (contiguous in the cache) into a shared-memory ring with bulk
+// copies; eight compute warps consume the ring with the same arithmetic as
+// the split kernel above.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kStreamWarps = 8;
+constexpr int kStreamThreads = (kStreamWarps + 1) * 32;  // + one producer warp
+constexpr int kStageBytes = 32 * 1024;                   // K half + V half
+constexpr int kStreamStages = 5;
+
+enum : unsigned { SITE_DEC_FULL = 40, SITE_DEC_EMPTY, SITE_DEC_SEG };
+
+struct StreamParams {
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    uint16_t* o;
+    float* lse;
+    float* ws_o;
+    float* ws_lse;
+    int Hq, Hkv, Tk, group, chunks, nseg_max;
+    long long total, per_cta;
+    float scale_log2;
+    unsigned* status;
+    unsigned long long limit_ns;
+};
+
+struct StreamBars {
+    uint64_t full[kStreamStages], empty[kStreamStages];
+    uint64_t seg_in, seg_out;
+    int abort;
+};
+
+template <int D, int HC>
+struct StreamLayout {
+    static constexpr int LPK = D / 8;
+    static constexpr int KPL = 32 / LPK;
+    static constexpr int KW = KPL * kNK;
+    static constexpr int NV0 = kNK * HC;
+    static constexpr int CK = kStageBytes / (2 * D * 2);  // keys per chunk
+    static_assert(CK == kStreamWarps * KW, "one warp iteration per warp per chunk");
+    static constexpr int kRingOff = 0;
+    static constexpr int kAccOff = kRingOff + kStreamStages * kStageBytes;
+    static constexpr int kPOff = kAccOff + kStreamWarps * HC * D * 4;
+    static constexpr int kMOff = kPOff + kStreamWarps * KPL * NV0 * 4;
+    static constexpr int kLOff = kMOff + kStreamWarps * HC * 4;
+    static constexpr int kBarOff = (kLOff + kStreamWarps * HC * 4 + 15) / 16 * 16;
+    static constexpr int kBytes = kBarOff + static_cast<int>(sizeof(StreamBars)) + 128;
+};
+
+struct Segment {
+    long long u;
+    int k0, k1;
+};
+
+// Next fragment [k0, k1) of unit u inside the virtual key range [v, v1).
+__device__ __forceinline__ bool next_segment(long long& v, long long v1, int Tk, Segment& sg) {
+    if (v >= v1) return false;
+    sg.u = v / Tk;
+    sg.k0 = static_cast<int>(v - sg.u * Tk);
+    const long long rem = v1 - v;
+    sg.k1 = static_cast<int>(rem < Tk - sg.k0 ? sg.k0 + rem : Tk);
+    v += sg.k1 - sg.k0;
+    return true;
+}
+
+template <int D, int HC>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+decode_stream_kernel(const StreamParams p) {
+    using L = StreamLayout<D, HC>;
+    constexpr int LPK = L::LPK, KPL = L::KPL, KW = L::KW, NV0 = L::NV0, CK = L::CK;
+    constexpr int NV = NV0 >= LPK ? NV0 / LPK : 1;
+    constexpr int kHalf = kStageBytes / 2;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    float (*s_acc)[HC][D] = reinterpret_cast<float (*)[HC][D]>(smem + L::kAccOff);
+    float (*s_p)[KPL][NV0] = reinterpret_cast<float (*)[KPL][NV0]>(smem + L::kPOff);
+    float (*s_m)[HC] = reinterpret_cast<float (*)[HC]>(smem + L::kMOff);
+    float (*s_l)[HC] = reinterpret_cast<float (*)[HC]>(smem + L::kLOff);
+    StreamBars* bars = reinterpret_cast<StreamBars*>(smem + L::kBarOff);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStreamStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], kStreamWarps);
+        }
+        mbar_init(&bars->seg_in, kStreamWarps);
+        mbar_init(&bars->seg_out, kStreamWarps);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitGuard g{p.status, &bars->abort, p.limit_ns};
+    const long long v_begin = static_cast<long long>(blockIdx.x) * p.per_cta;
+    const long long v_end = v_begin + p.per_cta < p.total ? v_begin + p.per_cta : p.total;
+
+    if (warp == kStreamWarps) {
+        // Producer: bulk-copy every chunk of this CTA's slice into the ring.
+        if (lane == 0) {
+            uint32_t it = 0;
+            long long v = v_begin;
+            Segment sg;
+            while (next_segment(v, v_end, p.Tk, sg)) {
+                const long long pair = sg.u / p.chunks;
+                for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
+                    const int n = min(CK, sg.k1 - kc);
+                    const int s = it % kStreamStages;
+                    if (it >= (uint32_t)kStreamStages &&
+                        !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY))
+                        goto drain;
+                    const uint32_t bytes = static_cast<uint32_t>(n) * D * 2;
+                    const int64_t row = pair * p.Tk + kc;
+                    uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
+                    mbar_arrive_expect_tx(&bars->full[s], 2 * bytes);
+                    bulk_load(stage, p.k + row * D, bytes, &bars->full[s]);
+                    bulk_load(stage + kHalf, p.v + row * D, bytes, &bars->full[s]);
+                }
+            }
+            goto out;
+        drain:
+            for (uint32_t i = (it > (uint32_t)kStreamStages ? it - kStreamStages : 0); i < it; ++i) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&bars->full[i % kStreamStages], (i / kStreamStages) & 1))
+                    if (global_timer_ns() - t0 > 200000000ull) break;
+            }
+        out:;
+        }
+    } else {
+        const int grp = lane / LPK, sub = lane % LPK;
+        uint32_t it = 0, nseg = 0;
+        long long v = v_begin;
+        Segment sg;
+        while (next_segment(v, v_end, p.Tk, sg)) {
+            const long long pair = sg.u / p.chunks;
+            const int chunk = static_cast<int>(sg.u - pair * p.chunks);
+            const int b = static_cast<int>(pair / p.Hkv), hkv = static_cast<int>(pair % p.Hkv);
+            const int hq0 = hkv * p.group + chunk * HC;
+            float qf[HC][8];
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                const uint16_t* qp = p.q + (static_cast<int64_t>(b) * p.Hq + hq0 + h) * D + sub * 8;
+                unpack8(*reinterpret_cast<const uint4*>(qp), qf[h]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
+            }
+            float m[HC], acc[HC][8], lsum[NV];
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                m[h] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
+            }
+#pragma unroll
+            for (int r = 0; r < NV; ++r) lsum[r] = 0.0f;
+
+            for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
+                const int n = min(CK, sg.k1 - kc);
+                const int s = it % kStreamStages;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[s], (it / kStreamStages) & 1, g,
+                                                       SITE_DEC_FULL)))
+                    goto done;
+                const uint8_t* ks = smem + L::kRingOff + s * kStageBytes;
+                const uint8_t* vs = ks + kHalf;
+                const int kb = warp * KW;
+                uint4 kr[kNK], vr[kNK];
+#pragma unroll
+                for (int nn = 0; nn < kNK; ++nn) {
+                    const int key = kb + nn * KPL + grp;
+                    if (key < n) {
+                        kr[nn] = *reinterpret_cast<const uint4*>(ks + key * D * 2 + sub * 16);
+                        vr[nn] = *reinterpret_cast<const uint4*>(vs + key * D * 2 + sub * 16);
+                    } else {
+                        kr[nn] = make_uint4(0, 0, 0, 0);
+                        vr[nn] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                float part[NV0];
+#pragma unroll
+                for (int nn = 0; nn < kNK; ++nn) {
+                    float kf[8];
+                    unpack8(kr[nn], kf);
+#pragma unroll
+                    for (int h = 0; h < HC; ++h) {
+                        float sacc = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) sacc = fmaf(qf[h][e], kf[e], sacc);
+                        part[nn * HC + h] = sacc;
+                    }
+                }
+                group_reduce_scatter<NV0, LPK>(part, lane);
+                float x[NV];
+                int hown[NV];
+                bool need = false;
+#pragma unroll
+                for (int r = 0; r < NV; ++r) {
+                    const int idx = own_index<NV0, LPK>(sub, r);
+                    hown[r] = idx % HC;
+                    const int key = kb + (idx / HC) * KPL + grp;
+                    x[r] = key < n ? part[r] : -INFINITY;
+                    float mh = m[0];
+#pragma unroll
+                    for (int h = 1; h < HC; ++h) mh = (hown[r] == h) ? m[h] : mh;
+                    need |= x[r] > mh + kRescaleThreshold;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int h = 0; h < HC; ++h) {
+                        float cm = -INFINITY;
+#pragma unroll
+                        for (int r = 0; r < NV; ++r) cm = (hown[r] == h) ? fmaxf(cm, x[r]) : cm;
+                        cm = warp_allmax(cm);
+                        const float mnew = fmaxf(m[h], cm);
+                        const float alpha = (m[h] == -INFINITY) ? 0.0f : ex2_approx(m[h] - mnew);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[h][e] *= alpha;
+#pragma unroll
+                        for (int r = 0; r < NV; ++r) lsum[r] = (hown[r] == h) ? lsum[r] * alpha : lsum[r];
+                        m[h] = mnew;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < NV; ++r) {
+                    float mh = m[0];
+#pragma unroll
+                    for (int h = 1; h < HC; ++h) mh = (hown[r] == h) ? m[h] : mh;
+                    const float pr = (x[r] == -INFINITY) ? 0.0f : ex2_approx(x[r] - mh);
+                    lsum[r] += pr;
+                    if (own_canonical<NV0, LPK>(sub)) s_p[warp][grp][own_index<NV0, LPK>(sub, r)] = pr;
+                }
+                __syncwarp();
+                float pall[NV0];
+#pragma unroll
+                for (int i = 0; i < NV0; i += 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(&s_p[warp][grp][i]);
+                    pall[i] = t.x; pall[i + 1] = t.y; pall[i + 2] = t.z; pall[i + 3] = t.w;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nn = 0; nn < kNK; ++nn) {
+                    float vf[8];
+                    unpack8(vr[nn], vf);
+#pragma unroll
+                    for (int h = 0; h < HC; ++h) {
+                        const float pw = pall[nn * HC + h];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+                    }
+                }
+                // Every value read from the stage has been used: release it.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->empty[s]);
+            }
+
+            // Segment end: merge lane groups, then warps (block-merge rule).
+#pragma unroll
+            for (int mask = LPK; mask < 32; mask <<= 1) {
+#pragma unroll
+                for (int h = 0; h < HC; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], mask);
+            }
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                float t = 0.0f;
+                if (own_canonical<NV0, LPK>(sub)) {
+#pragma unroll
+                    for (int r = 0; r < NV; ++r)
+                        t += ((own_index<NV0, LPK>(sub, r) % HC) == h) ? lsum[r] : 0.0f;
+                }
+                const float lw = warp_allsum(t);
+                if (lane == 0) {
+                    s_m[warp][h] = m[h];
+                    s_l[warp][h] = lw;
+                }
+            }
+            if (lane < LPK) {
+#pragma unroll
+                for (int h = 0; h < HC; ++h)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s_acc[warp][h][sub * 8 + e] = acc[h][e];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->seg_in);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->seg_in, nseg & 1, g, SITE_DEC_SEG)))
+                goto done;
+            {
+                const bool whole = sg.k0 == 0 && sg.k1 == p.Tk;
+                const long long seg = static_cast<long long>(blockIdx.x) - (sg.u * p.Tk) / p.per_cta;
+                for (int idx = threadIdx.x; idx < HC * D; idx += kStreamWarps * 32) {
+                    const int h = idx / D, d = idx % D;
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < kStreamWarps; ++w) M = fmaxf(M, s_m[w][h]);
+                    float Ls = 0.0f, O = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kStreamWarps; ++w) {
+                        const float wt = (s_m[w][h] == -INFINITY) ? 0.0f : ex2_approx(s_m[w][h] - M);
+                        Ls = fmaf(s_l[w][h], wt, Ls);
+                        O = fmaf(s_acc[w][h][d], wt, O);
+                    }
+                    const float out = O / Ls;
+                    const float lse2 = M + __log2f(Ls);
+                    if (whole) {
+                        const int64_t row = static_cast<int64_t>(b) * p.Hq + hq0 + h;
+                        const uint32_t pk = pack_bf16x2(out, 0.0f);
+                        p.o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
+                        if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
+                    } else {
+                        const int64_t slot = (sg.u * p.nseg_max + seg) * HC + h;
+                        p.ws_o[slot * D + d] = out;
+                        if (d == 0) p.ws_lse[slot] = lse2;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->seg_out);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->seg_out, nseg & 1, g, SITE_DEC_SEG)))
+                goto done;
+            ++nseg;
+        }
+    done:;
+    }
+    __syncthreads();
+}
+
+// Merge the fragments of the units that slice boundaries cut; units a single
+// CTA covered were written directly.
+template <int D>
+__global__ void __launch_bounds__(D)
+decode_stream_combine_kernel(const StreamParams p, int hc) {
+    const int row = blockIdx.x;
+    const int d = threadIdx.x;
+    const int b = row / p.Hq, hq = row - b * p.Hq;
+    const int hkv = hq / p.group, hl = hq - hkv * p.group;
+    const long long u = (static_cast<long long>(b) * p.Hkv + hkv) * p.chunks + hl / hc;
+    const int h = hl % hc;
+    const long long c0 = (u * p.Tk) / p.per_cta;
+    const long long c1 = (u * p.Tk + p.Tk - 1) / p.per_cta;
+    const int nseg = static_cast<int>(c1 - c0 + 1);
+    if (nseg == 1) return;
+    float M = -INFINITY;
+    for (int s = 0; s < nseg; ++s) M = fmaxf(M, p.ws_lse[(u * p.nseg_max + s) * hc + h]);
+    float Ls = 0.0f, acc = 0.0f;
+    for (int s = 0; s < nseg; ++s) {
+        const int64_t slot = (u * p.nseg_max + s) * hc + h;
+        const float w = ex2_approx(p.ws_lse[slot] - M);
+        Ls += w;
+        acc = fmaf(w, p.ws_o[slot * D + d], acc);
+    }
+    const uint32_t pk = pack_bf16x2(acc / Ls, 0.0f);
+    p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
+    if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
+}
+
+template <int D, int HC>
+cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
+    using L = StreamLayout<D, HC>;
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, HC>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    decode_stream_kernel<D, HC><<<grid, kStreamThreads, L::kBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_stream_d(const StreamParams& p, int hc, int grid, cudaStream_t st) {
+    switch (hc) {
+        case 8: return launch_stream<D, 8>(p, grid, st);
+        case 4: return launch_stream<D, 4>(p, grid, st);
+        case 2: return launch_stream<D, 2>(p, grid, st);
+        default: return launch_stream<D, 1>(p, grid, st);
+    }
+}
+
+// Slice geometry shared by the workspace size and the launch.
+struct StreamGeom {
+    long long total, per_cta;
+    int grid, nseg_max, hc, chunks;
+};
+
+StreamGeom stream_geom(const Shape& s, int num_sms) {
+    StreamGeom g;
+    const int group = s.Hq / s.Hkv;
+    g.hc = heads_per_cta(group);
+    g.chunks = group / g.hc;
+    g.total = static_cast<long long>(s.B) * s.Hkv * g.chunks * s.Tk;
+    g.per_cta = (g.total + num_sms - 1) / num_sms;
+    g.grid = static_cast<int>((g.total + g.per_cta - 1) / g.per_cta);
+    g.nseg_max = static_cast<int>((s.Tk + g.per_cta - 1) / g.per_cta) + 1;
+    return g;
+}
+
+}  // namespace
+
+size_t decode_stream_workspace_bytes(const Shape& s, int num_sms) {
+    const StreamGeom g = stream_geom(s, num_sms);
+    const size_t slots = static_cast<size_t>(s.B) * s.Hq * g.nseg_max;
+    return slots * s.D * sizeof(float) + slots * sizeof(float) + 256;
+}
+
+cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                      uint16_t* o, float* lse, float* ws, const Shape& s,
+                                      const LaunchEnv& env, int* grid_out, int* kernels_launched) {
+    const StreamGeom g = stream_geom(s, env.num_sms);
+    StreamParams p;
+    p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse;
+    const size_t slots = static_cast<size_t>(s.B) * s.Hq * g.nseg_max;
+    p.ws_o = ws;
+    p.ws_lse = ws + slots * s.D;
+    p.Hq = s.Hq; p.Hkv = s.Hkv; p.Tk = s.Tk; p.group = s.Hq / s.Hkv; p.chunks = g.chunks;
+    p.nseg_max = g.nseg_max;
+    p.total = g.total;
+    p.per_cta = g.per_cta;
+    p.scale_log2 = s.scale * 1.4426950408889634f;
+    p.status = env.status;
+    p.limit_ns = env.wait_limit_ns;
+    cudaError_t e = (s.D == 64) ? launch_stream_d<64>(p, g.hc, g.grid, env.stream)
+                                : launch_stream_d<128>(p, g.hc, g.grid, env.stream);
+    int launched = 1;
+    if (e == cudaSuccess && g.nseg_max > 1) {
+        const int rows = s.B * s.Hq;
+        if (s.D == 64)
+            decode_stream_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, g.hc);
+        else
+            decode_stream_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, g.hc);
+        e = cudaGetLastError();
+        launched = 2;
+    }
+    if (grid_out) *grid_out = g.grid;
+    if (kernels_launched) *kernels_launched = launched;
+    return e;
+}
+
 }  // namespace attn

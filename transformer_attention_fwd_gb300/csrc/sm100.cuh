@@ -117,6 +117,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
            "r"(c0), "r"(c1), "r"(c2) : "memory");
 }
 
+// Contiguous bulk copy global -> shared (no tensor map).  dst, src 16-byte
+// aligned, bytes a multiple of 16; completion counted on bar.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+           "r"(smem_u32(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Tensor memory
 // ---------------------------------------------------------------------------
