@@ -44,7 +44,7 @@ DECODE_SOURCES = ["transformer_attention_fwd_gb300/csrc/decode_bf16.cu",
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-secondary", action="store_true",
@@ -113,7 +113,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", self.gpu_id],
+                 "-lms", "50", "-i", self.gpu_id],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -340,11 +340,13 @@ def run_secondary(args, attn, peaks, flush):
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     out["decode"] = {
         "workload": DECODE, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
-        "algorithmic_bytes": w.io_bytes(), "splits": splits, "kernels_per_step": kernels,
+        "algorithmic_bytes": w.io_bytes(),
+        "mode": "stream-K, one key slice per SM" if splits == 0 else f"{splits} splits",
+        "kernels_per_step": kernels,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4),
                      "traffic": load_traffic("decode_b64_tk4096", DECODE_SOURCES),
-                     "note": "step time includes the split kernel and the combine kernel"},
+                     "note": "step time includes the stream kernel and the fragment combine kernel"},
     }
     del q, k, v, o, lse
     # GPT-2-small-shaped causal prefill, D = 64.
