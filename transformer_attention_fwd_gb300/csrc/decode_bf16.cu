@@ -528,6 +528,8 @@ __device__ __forceinline__ bool next_segment(long long& v, long long v1, int Tk,
     return true;
 }
 
+// Nine warps put three on one SM sub-partition, whose 16K registers cap a
+// thread at 168 (HC = 8 spills a little; splitting the heads would re-read K/V).
 template <int D, int HC>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 decode_stream_kernel(const StreamParams p) {
