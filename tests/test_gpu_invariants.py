@@ -136,3 +136,22 @@ def test_shift_of_keys_moves_lse_only():
     check_status(a)
     o_ref, lse_ref = oracle.attention_f64(q, k2, v, True)
     compare(o2, lse2, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
+
+
+@pytest.mark.parametrize("causal,Tq", [(True, 512), (False, 512), (False, 1)])
+def test_rising_scores_take_the_exact_path(causal, Tq):
+    """Scores that grow along the key axis by far more than 2^64 (in base 2)
+    between the first and the last key tile force the kernels off their
+    fast path (weights against the first tile's maximum) onto the exact
+    max-and-rescale path; the result must still match the oracle."""
+    a = attn()
+    g = torch.Generator().manual_seed(69)
+    Tk, D = 512, 64
+    ramp = torch.linspace(0.0, 10.0, Tk)[None, None, :, None]
+    q = (torch.ones(1, 2, Tq, D) + 0.3 * torch.randn(1, 2, Tq, D, generator=g)).to(torch.bfloat16)
+    k = (ramp + 0.5 * torch.randn(1, 2, Tk, D, generator=g)).to(torch.bfloat16)
+    v = torch.randn(1, 2, Tk, D, generator=g).to(torch.bfloat16)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=causal)
+    check_status(a)
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, causal)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, 1e-3 * max(1.0, float(abs(lse_ref).max())) / 10)

@@ -24,7 +24,9 @@
 // issue order per key tile j is
 //     S0(j)  PV1(j-1)  S1(j)  PV0(j)
 // so each softmax warpgroup works on one tile while the tensor core runs the
-// other tile's products.
+// other tile's products.  The softmax computes a row maximum only on a row's
+// first tile and on the rare tile whose weights outgrow 2^64; every other
+// tile is weighted against the running reference directly.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cmath>
@@ -40,11 +42,10 @@ constexpr int BM = 128;                  // query rows per tile = TMEM lanes
 constexpr int BN = 128;                  // keys per K/V tile
 constexpr int NQT = 2;                   // query tiles per work item
 constexpr int kItemRows = BM * NQT;
-constexpr int kThreads = 640;  // 4 control warps + 4 softmax warpgroups
+constexpr int kThreads = 384;
 constexpr int kBoxCols = 64;             // 64 bf16 = one 128-byte swizzle row
 constexpr int kBoxBytes = kBoxCols * BM * 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Wait sites reported in the status word when a wait times out.
@@ -59,31 +60,25 @@ struct Cfg {
     static constexpr int kChunks = D / kBoxCols;
     static constexpr int kTileBytes = kChunks * kBoxBytes;  // 128 rows x D bf16
     static constexpr int kQStages = (D == 128) ? 1 : 2;    // Q buffers (2 query tiles each)
-    static constexpr int kKStages = (D == 128) ? 2 : 4;
+    static constexpr int kKStages = (D == 128) ? 3 : 4;
     static constexpr int kVStages = (D == 128) ? 2 : 4;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQStages * NQT * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
     static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
     static constexpr int kBarBytes = 256;
-    // Row-half exchange: [tile][half][3 slots][128 rows] floats.
-    static constexpr int kXchOff = kBarOff + kBarBytes;
-    static constexpr int kXchBytes = 2 * 2 * 3 * 128 * 4;
-    static constexpr int kSmemBytes = kXchOff + kXchBytes + 1024;  // + 1024-byte alignment slack
+    static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + 1024-byte alignment slack
     // Tensor-memory columns of the S/P and O accumulators of query tile t.
     __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
     __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
 };
 
-// Register split (setmaxnreg): 20 warps put 5 on each SM sub-partition, so
-// the CTA launches with 96 registers per thread (640 x 96 = 61440); the four
-// control warps drop to 56 and the sixteen softmax warps rise to 104:
-// 128 x 56 + 512 x 104 = 60416 <= 61440.
-constexpr int kLaunchRegs = 96;
-constexpr int kCtrlRegs = 56;
-constexpr int kSoftmaxRegs = 104;
-static_assert(128 * kCtrlRegs + 512 * kSoftmaxRegs <= kThreads * kLaunchRegs,
-              "register split too large");
+// Register split (setmaxnreg): the CTA launches with 168 registers per thread
+// (384 x 168 = 64512); the four control warps drop to 64 and the eight
+// softmax warps rise to 216: 128 x 64 + 256 x 216 = 63488 <= 64512.
+constexpr int kCtrlRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * 168, "register split too large");
 
 // Share of the exponentials of an unmasked tile evaluated by the polynomial
 // (exp2_poly_x2) instead of the MUFU unit: pairs with
@@ -102,7 +97,6 @@ struct Bars {
     uint64_t k_full[4], k_empty[4];
     uint64_t v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-    uint64_t xch[2];  // the two row halves of a query tile meet here
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -375,7 +369,7 @@ __device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2,
     uint64_t acc_e[2] = {0, 0};
     float acc_r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[c][2 * i]),
@@ -402,27 +396,36 @@ __device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2,
     sum_rounded = (acc_r[0] + acc_r[1]) + (acc_r[2] + acc_r[3]);
 }
 
-// Softmax for one half of a query tile: warpgroup grp = 2 * t + h owns
-// columns [64h, 64h + 64) of every row of query tile t (thread = row = TMEM
-// lane).  The two halves of a row exchange their maxima (and, at the end,
-// their row sums) through shared memory behind a bounded mbarrier, write
-// their own 32 packed P columns, and rescale and store their own D/2 output
-// columns.
+// Load this thread's row of an S tile (128 fp32 columns) from tensor memory;
+// on a tile that straddles the diagonal or the end of the keys, keys past
+// this row's last visible key become -inf.
+__device__ __forceinline__ void load_scores(uint32_t (&r)[4][32], uint32_t taddr, bool masked,
+                                            int kbase, int lim) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, r[c]);
+    tmem_wait_ld(r[0]);
+    reg_order(r[1]);
+    reg_order(r[2]);
+    reg_order(r[3]);
+    if (masked) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (kbase + 32 * c + i > lim) r[c][i] = __float_as_uint(-INFINITY);
+    }
+}
+
 template <int D>
-__device__ void softmax_half(int grp, Bars* bars, float* xch, uint32_t tmem,
-                             const PrefillParams& p, const WaitGuard& g) {
+__device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams& p,
+                           const WaitGuard& g) {
     using C = Cfg<D>;
-    const int t = grp >> 1, h = grp & 1;
+    const int row_in_tile = threadIdx.x - 128 * (1 + t);  // = TMEM lane
     const int warp = threadIdx.x / 32;
-    const int row_in_tile = 32 * (warp & 3) + (threadIdx.x & 31);  // = TMEM lane
     const uint32_t lane_addr = tmem_lane_base(tmem, warp);
-    const uint32_t colS = C::col_s(t) + 64u * h;              // 64 score columns
-    const uint32_t colP = C::col_s(t) + 32u * h;              // 32 packed P columns
-    const uint32_t colO = C::col_o(t) + (D / 2) * h;          // D/2 output columns
-    float* mine = xch + ((t * 2 + h) * 3) * 128 + row_in_tile;
-    const float* other = xch + ((t * 2 + (1 - h)) * 3) * 128 + row_in_tile;
+    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
     const int off = p.Tk - p.Tq;
-    uint32_t s_cnt = 0, o_cnt = 0, x_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;
 
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
         const int idx = snake_item(k, p.n_items);
@@ -432,112 +435,95 @@ __device__ void softmax_half(int grp, Bars* bars, float* xch, uint32_t tmem,
         if (n == 0) continue;
         const int r0 = it.qb * kItemRows + t * BM;
         const int row = r0 + row_in_tile;
+        // Last visible key of this row and of the tile's first row.
         const int lim = p.causal ? min(row + off, p.Tk - 1) : p.Tk - 1;
         const int lim_first = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
         float m = -INFINITY, l = 0.0f, lr = 0.0f;
 
         for (int j = 0; j < n; ++j) {
+            // Warp-uniform outcome: tcgen05.ld below needs the whole warp.
             if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], s_cnt & 1, g, SITE_S_FULL)))
                 return;
             ++s_cnt;
             tc_fence_after_sync();
-            uint32_t r[4][32];  // chunks 0, 1 used
-            tmem_ld32(lane_addr + colS, r[0]);
-            tmem_ld32(lane_addr + colS + 32, r[1]);
-            tmem_wait_ld(r[0]);
-            reg_order(r[1]);
-            const int kbase = j * BN + 64 * h;
-            const bool masked = j * BN + BN - 1 > lim_first;  // tile straddles the diagonal or Tk
-            if (masked) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (kbase + 32 * c + i > lim) r[c][i] = __float_as_uint(-INFINITY);
+            uint32_t r[4][32];
+            const int kbase = j * BN;
+            const bool masked = kbase + BN - 1 > lim_first;  // straddles the diagonal or Tk
+            load_scores(r, lane_addr + colS, masked, kbase, lim);
+            // Fast path: weights against the running reference m without a
+            // row maximum.  bf16 P and the fp32 sums and accumulators have
+            // fp32's exponent range, so weights far above 1 lose no relative
+            // precision; a tile whose exact weight sum exceeds 2^64 (or is not
+            // finite) means m must move, and it is redone on the exact path.
+            // The first tile of a row always takes the exact path.
+            float sum_e = 0.0f, sum_r = 0.0f;
+            bool exact = (m == -INFINITY);
+            if (!__any_sync(0xffffffffu, exact)) {
+                if (masked)
+                    row_exp2<false>(r, p.scale_log2, -m, sum_e, sum_r);
+                else
+                    row_exp2<true>(r, p.scale_log2, -m, sum_e, sum_r);
+                exact = !(sum_e <= 0x1p64f);
+                if (__any_sync(0xffffffffu, exact))  // S was packed in place: reload it
+                    load_scores(r, lane_addr + colS, masked, kbase, lim);
             }
-            float mc[4];
+            if (__any_sync(0xffffffffu, exact)) {
+                // Exact path: row maximum (four independent 3-input max chains),
+                // move m to the running maximum and rescale l, lr and O.
+                float mc[4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c = q4 >> 1, b = (q4 & 1) * 16;
-                float a = fmaxf(__uint_as_float(r[c][b]), __uint_as_float(r[c][b + 1]));
+                for (int c = 0; c < 4; ++c) {
+                    float a = fmaxf(__uint_as_float(r[c][0]), __uint_as_float(r[c][1]));
 #pragma unroll
-                for (int i = 2; i < 16; i += 2)
-                    a = fmax3(a, __uint_as_float(r[c][b + i]), __uint_as_float(r[c][b + i + 1]));
-                mc[q4] = a;
-            }
-            const float mh = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-            mine[0] = mh;
-            mbar_arrive(&bars->xch[t]);
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->xch[t], x_cnt & 1, g, SITE_S_FULL)))
-                return;
-            ++x_cnt;
-            const float mx = fmaxf(mh, other[0]);
-            const float m_new = fmaxf(m, mx * p.scale_log2);
-            const bool need = m_new > m + kRescaleThreshold;
-            const bool rescale = __any_sync(0xffffffffu, need);
-            float alpha = 1.0f;
-            if (rescale) {
+                    for (int i = 2; i < 32; i += 2)
+                        a = fmax3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
+                    mc[c] = a;
+                }
+                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
+                const float m_new = fmaxf(m, mx * p.scale_log2);
                 const float m_use = (m_new == -INFINITY) ? m : m_new;
-                alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_use);
+                const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_use);
                 l *= alpha;
                 lr *= alpha;
+                if (j > 0) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_addr + colO + 32 * c, ov);
+                        tmem_wait_ld(ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(lane_addr + colO + 32 * c, ov);
+                    }
+                }
                 m = m_use;
+                const float neg_m = (m == -INFINITY) ? 0.0f : -m;
+                if (masked)
+                    row_exp2<false>(r, p.scale_log2, neg_m, sum_e, sum_r);
+                else
+                    row_exp2<true>(r, p.scale_log2, neg_m, sum_e, sum_r);
             }
-            const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-            // P = 2^(s*scale*log2e - m) as packed bf16 pairs.  Two row sums:
-            // l (exact weights) gives the log-sum-exp; lr adds the bf16-rounded
-            // weights, i.e. exactly the values the P.V product multiplies, and
-            // normalises O so its weights sum to 1.  Masked tiles use the MUFU
-            // exponential only, so masked weights are exactly 0.
-            float sum_e, sum_r;
-            if (masked)
-                row_exp2<false>(r, p.scale_log2, neg_m, sum_e, sum_r);
-            else
-                row_exp2<true>(r, p.scale_log2, neg_m, sum_e, sum_r);
-            // Chunk c's 16 packed columns hold keys 64h + 32c .. 64h + 32c + 31.
-            tmem_st16(lane_addr + colP, r[0]);
-            tmem_st16(lane_addr + colP + 16, r[1]);
+            // Chunk c's 16 packed columns hold keys 32c .. 32c+31.
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_st16(lane_addr + colS + 16 * c, r[c]);
+            tmem_wait_st();
             l += sum_e;
             lr += sum_r;
-            // Rescale this half of O when the running maximum moved.  The
-            // previous P.V into O completed before S of this tile did (they
-            // were issued in that order), and the next one waits for p_full.
-            if (rescale && j > 0) {
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_addr + colO + 32 * c, ov);
-                    tmem_wait_ld(ov);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(lane_addr + colO + 32 * c, ov);
-                }
-            }
-            tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(&bars->p_full[t]);
         }
 
-        // Epilogue: O = O_acc / lr -> bf16; lse = (m + log2 l) * ln 2, with
-        // both halves' sums.
+        // Epilogue: O = O_acc / lr -> bf16; lse = (m + log2 l) * ln 2.
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], o_cnt & 1, g, SITE_O_FULL)))
             return;
         ++o_cnt;
         tc_fence_after_sync();
-        mine[128] = lr;
-        mine[256] = l;
-        mbar_arrive(&bars->xch[t]);
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->xch[t], x_cnt & 1, g, SITE_O_FULL)))
-            return;
-        ++x_cnt;
-        const float lr_row = lr + other[128];
-        const float l_row = l + other[256];
-        const float inv_l = 1.0f / lr_row;
+        const float inv_l = 1.0f / lr;
         const bool in_range = row < p.Tq;
-        uint16_t* orow = p.o + (static_cast<int64_t>(it.bh) * p.Tq + row) * D + (D / 2) * h;
+        uint16_t* orow = p.o + (static_cast<int64_t>(it.bh) * p.Tq + row) * D;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
             tmem_ld32(lane_addr + colO + 32 * c, ov);
             tmem_wait_ld(ov);
@@ -553,8 +539,8 @@ __device__ void softmax_half(int grp, Bars* bars, float* xch, uint32_t tmem,
                     dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
         }
-        if (h == 0 && in_range && p.lse != nullptr)
-            p.lse[static_cast<int64_t>(it.bh) * p.Tq + row] = (m + __log2f(l_row)) * kLn2;
+        if (in_range && p.lse != nullptr)
+            p.lse[static_cast<int64_t>(it.bh) * p.Tq + row] = (m + __log2f(l)) * kLn2;
         tc_fence_before_sync();
         mbar_arrive(&bars->o_empty[t]);
     }
@@ -584,10 +570,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->p_full[t], 2 * BM);
+            mbar_init(&bars->p_full[t], BM);
             mbar_init(&bars->o_full[t], 1);
-            mbar_init(&bars->o_empty[t], 2 * BM);
-            mbar_init(&bars->xch[t], 2 * BM);
+            mbar_init(&bars->o_empty[t], BM);
         }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -619,8 +604,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
     } else {
         regs_increase<kSoftmaxRegs>();
-        softmax_half<D>((warp - 4) / 4, bars, reinterpret_cast<float*>(smem + C::kXchOff), tmem,
-                        p, g);
+        softmax_wg<D>((warp - 4) / 4, bars, tmem, p, g);
     }
 
     tc_fence_before_sync();
