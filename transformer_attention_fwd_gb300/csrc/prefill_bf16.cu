@@ -13,7 +13,7 @@
 // GB300 mapping (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer for Q and K tiles        (one elected lane)
 //   warp 3      TMA producer for V tiles              (one elected lane)
-//   warp 1      MMA issuer                            (one elected lane)
+//   warp 1      MMA issuer        (whole warp, converged; elect.sync issues)
 //   warp 2      tensor-memory allocator
 //   warps 4-7   softmax warpgroup for query tile 0    (thread = row = TMEM lane)
 //   warps 8-11  softmax warpgroup for query tile 1
@@ -194,6 +194,13 @@ __device__ __forceinline__ void wait_quiet(uint64_t* bar, uint32_t parity, uint6
 
 constexpr uint64_t kDrainLimitNs = 200ull * 1000ull * 1000ull;
 
+// A wait taken by every lane of the MMA warp; the result is made warp-uniform
+// so the warp stays converged for the elected MMA issue.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitGuard& g,
+                                          unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, g, site));
+}
+
 // ----------------------------------------------------------------------------
 // Roles
 // ----------------------------------------------------------------------------
@@ -289,7 +296,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
         const int n0 = it.n[0], n1 = it.n[1];
         const int nkv = max(n0, n1);
         const int qs = q_it % C::kQStages;
-        if (!mbar_wait(&bars->q_full[qs], (q_it / C::kQStages) & 1, g, SITE_Q_FULL)) goto drain;
+        if (!warp_wait(&bars->q_full[qs], (q_it / C::kQStages) & 1, g, SITE_Q_FULL)) goto drain;
         ++q_it;
         tc_fence_after_sync();
         const uint32_t q_base = smem_u32(smem + C::kQOff + qs * NQT * C::kTileBytes);
@@ -301,7 +308,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
             const uint32_t k_smem = k_base + ks * C::kTileBytes;
             const uint32_t v_smem = v_base + vs * C::kTileBytes;
             if (j < nkv) {
-                if (!mbar_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
+                if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
                 if (j < n0) {
                     issue_qk<D>(tmem + C::col_s(0), q_base, k_smem);
@@ -311,12 +318,12 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
             if (j >= 1 && j - 1 < n1) {  // PV1(j-1)
                 const uint32_t ip = itj - 1;
                 const int pvs = ip % C::kVStages;
-                if (!mbar_wait(&bars->p_full[1], p_cnt[1] & 1, g, SITE_P_FULL)) goto drain;
+                if (!warp_wait(&bars->p_full[1], p_cnt[1] & 1, g, SITE_P_FULL)) goto drain;
                 ++p_cnt[1];
-                if (!mbar_wait(&bars->v_full[pvs], (ip / C::kVStages) & 1, g, SITE_V_FULL))
+                if (!warp_wait(&bars->v_full[pvs], (ip / C::kVStages) & 1, g, SITE_V_FULL))
                     goto drain;
                 if (j - 1 == 0 && o_cnt[1] > 0 &&
-                    !mbar_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
+                    !warp_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
                     goto drain;
                 tc_fence_after_sync();
                 issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
@@ -335,11 +342,11 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                 mma_commit(&bars->k_empty[ks]);
                 if (j == nkv - 1) mma_commit(&bars->q_empty[qs]);
                 if (j < n0) {  // PV0(j)
-                    if (!mbar_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
+                    if (!warp_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
                     ++p_cnt[0];
-                    if (!mbar_wait(&bars->v_full[vs], vph, g, SITE_V_FULL)) goto drain;
+                    if (!warp_wait(&bars->v_full[vs], vph, g, SITE_V_FULL)) goto drain;
                     if (j == 0 && o_cnt[0] > 0 &&
-                        !mbar_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
+                        !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
                     issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_smem, j > 0);
@@ -600,7 +607,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         } else if (warp == 3) {
             if (lane == 0) producer_v<D>(&tmV, smem, bars, p, g);
         } else if (warp == 1) {
-            if (lane == 0) mma_issuer<D>(smem, bars, tmem, p, g);
+            mma_issuer<D>(smem, bars, tmem, p, g);
         }
     } else {
         regs_increase<kSoftmaxRegs>();
@@ -653,20 +660,22 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t lane_addr = tmem_lane_base(tmem, warp);
     bool ok = true;
 
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(&bars->q_full[0], 3 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_2d(sa + c * kBoxBytes, &tmA, &bars->q_full[0], c * kBoxCols, 0);
-            tma_load_2d(sb + c * kBoxBytes, &tmB, &bars->q_full[0], c * kBoxCols, 0);
-            tma_load_2d(sv + c * kBoxBytes, &tmV, &bars->q_full[0], c * kBoxCols, 0);
+    if (warp == 0) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&bars->q_full[0], 3 * C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_2d(sa + c * kBoxBytes, &tmA, &bars->q_full[0], c * kBoxCols, 0);
+                tma_load_2d(sb + c * kBoxBytes, &tmB, &bars->q_full[0], c * kBoxCols, 0);
+                tma_load_2d(sv + c * kBoxBytes, &tmV, &bars->q_full[0], c * kBoxCols, 0);
+            }
         }
-        if (mbar_wait(&bars->q_full[0], 0, g, SITE_DIAG_LOAD)) {
+        __syncwarp();
+        if (warp_wait(&bars->q_full[0], 0, g, SITE_DIAG_LOAD)) {
             tc_fence_after_sync();
             issue_qk<D>(tmem, smem_u32(sa), smem_u32(sb));
             mma_commit(&bars->s_full[0]);
         }
     }
-    __syncwarp();
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], 0, g, SITE_DIAG_MMA));
     if (ok) {
         tc_fence_after_sync();
@@ -698,12 +707,11 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (threadIdx.x == 0 && ok && !bars->abort) {
+    if (warp == 0 && __all_sync(0xffffffffu, ok && !bars->abort)) {
         tc_fence_after_sync();
         issue_pv<D>(tmem + 128, tmem, smem_u32(sv), false);
         mma_commit(&bars->s_full[0]);
     }
-    __syncwarp();
     ok = ok && !bars->abort;
     if (__all_sync(0xffffffffu, ok && mbar_wait(&bars->s_full[0], 1, g, SITE_DIAG_MMA))) {
         tc_fence_after_sync();
@@ -716,7 +724,7 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int i = 0; i < 32; ++i) o_out[row * D + 32 * c + i] = __uint_as_float(ov[i]);
         }
     }
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
         mma_commit(&bars->drain);
         wait_quiet(&bars->drain, 0, kDrainLimitNs);
     }
