@@ -15,18 +15,20 @@
 //   warp 3      TMA producer for V tiles              (one elected lane)
 //   warp 1      MMA issuer        (whole warp, converged; elect.sync issues)
 //   warp 2      tensor-memory allocator
-//   warps 4-7   softmax warpgroup for query tile 0    (thread = row = TMEM lane)
-//   warps 8-11  softmax warpgroup for query tile 1
+//   warps 4-11  softmax: warp w owns TMEM lanes 32(w%4) + 16((w-4)/4) .. +15,
+//               i.e. 16 rows of each query tile, four threads per row
 // A work item is 256 query rows (two 128-row tiles) of one (b, hq).  Tensor
 // memory (512 columns x 128 lanes x 32 bit) holds S0, S1 (128 columns each),
 // O0, O1 (D columns each).  P overwrites the first 64 columns of its S tile as
 // packed bf16 and feeds the P.V MMA straight from tensor memory.  The MMA
 // issue order per key tile j is
 //     S0(j)  PV1(j-1)  S1(j)  PV0(j)
-// so each softmax warpgroup works on one tile while the tensor core runs the
-// other tile's products.  The softmax computes a row maximum only on a row's
-// first tile and on the rare tile whose weights outgrow 2^64; every other
-// tile is weighted against the running reference directly.
+// so the softmax works on one tile while the tensor core runs the other
+// tile's products; every tile is spread over two warps per SM sub-partition,
+// which halves the latency of its softmax against one warp per row quarter.
+// The softmax computes a row maximum only on a row's first tile and on the
+// rare tile whose weights outgrow 2^64; every other tile is weighted against
+// the running reference directly.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cmath>
@@ -43,6 +45,7 @@ constexpr int BN = 128;                  // keys per K/V tile
 constexpr int NQT = 2;                   // query tiles per work item
 constexpr int kItemRows = BM * NQT;
 constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;  // warps 4-11
 constexpr int kBoxCols = 64;             // 64 bf16 = one 128-byte swizzle row
 constexpr int kBoxBytes = kBoxCols * BM * 2;
 constexpr uint32_t kTmemCols = 512;
@@ -365,191 +368,256 @@ drain:
     wait_quiet(&bars->drain, 0, kDrainLimitNs);
 }
 
-// Exponentials of one row of a tile, packed to bf16 pairs in place:
-// r[c][0..15] receives the 16 packed pairs of chunk c (keys 32c .. 32c+31).
-// Returns the exact and the bf16-rounded row sums as packed pairs.
+// Softmax work of one warp on one S tile: 16 rows (TMEM lanes L0 .. L0+15)
+// x 128 keys.  Thread i holds rows a = L0 + i/4 and b = a + 8, and in each
+// 8-key chunk n the keys 8n + 2(i%4) and 8n + 2(i%4) + 1 of both rows
+// (registers 4n .. 4n+3 of the .16x256b load: a, a, b, b).  The four threads
+// of a row hold its 128 keys between them.
+
+// Exponentials 2^(s*scale - m) of one tile.  p receives the packed bf16 pairs
+// in .16x128b order (p[2n] row a, p[2n+1] row b, both P column 4n + i%4, i.e.
+// keys 8n + 2(i%4) and +1); se/sr receive this thread's exact and
+// bf16-rounded partial row sums.
 template <bool kPoly>
-__device__ __forceinline__ void row_exp2(uint32_t (&r)[4][32], float scale_log2, float neg_m,
-                                         float& sum_exact, float& sum_rounded) {
+__device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_log2,
+                                          float neg_ma, float neg_mb, uint32_t (&p)[32],
+                                          float (&se)[2], float (&sr)[2]) {
     const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-    const uint64_t nm2 = f2_pack(neg_m, neg_m);
-    uint64_t acc_e[2] = {0, 0};
-    float acc_r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint64_t nm2[2] = {f2_pack(neg_ma, neg_ma), f2_pack(neg_mb, neg_mb)};
+    uint64_t acc_e[2][2] = {{0, 0}, {0, 0}};
+    float acc_r[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int n = 0; n < 16; ++n) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[c][2 * i]),
-                                               __uint_as_float(r[c][2 * i + 1])), sc2, nm2);
-            float a, b;
-            if (kPoly && kPolyEvery > 0 && (i % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-                exp2_poly_x2(x2, a, b);
+        for (int r = 0; r < 2; ++r) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(s[4 * n + 2 * r]),
+                                               __uint_as_float(s[4 * n + 2 * r + 1])),
+                                       sc2, nm2[r]);
+            float e0, e1;
+            if (kPoly && kPolyEvery > 0 &&
+                (n % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
+                exp2_poly_x2(x2, e0, e1);
             } else {
                 float x0, x1;
                 f2_unpack(x2, x0, x1);
-                a = ex2_approx(x0);
-                b = ex2_approx(x1);
+                e0 = ex2_approx(x0);
+                e1 = ex2_approx(x1);
             }
-            const uint32_t pk = pack_bf16x2(a, b);
-            acc_e[i & 1] = f2_add(acc_e[i & 1], f2_pack(a, b));
-            add_bf16x2_to_f32(pk, acc_r[2 * (i & 1)], acc_r[2 * (i & 1) + 1]);
-            r[c][i] = pk;
+            const uint32_t pk = pack_bf16x2(e0, e1);
+            acc_e[r][n & 1] = f2_add(acc_e[r][n & 1], f2_pack(e0, e1));
+            add_bf16x2_to_f32(pk, acc_r[r][0], acc_r[r][1]);
+            p[2 * n + r] = pk;
         }
     }
-    float e0, e1, e2, e3;
-    f2_unpack(acc_e[0], e0, e1);
-    f2_unpack(acc_e[1], e2, e3);
-    sum_exact = (e0 + e1) + (e2 + e3);
-    sum_rounded = (acc_r[0] + acc_r[1]) + (acc_r[2] + acc_r[3]);
-}
-
-// Load this thread's row of an S tile (128 fp32 columns) from tensor memory;
-// on a tile that straddles the diagonal or the end of the keys, keys past
-// this row's last visible key become -inf.
-__device__ __forceinline__ void load_scores(uint32_t (&r)[4][32], uint32_t taddr, bool masked,
-                                            int kbase, int lim) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, r[c]);
-    tmem_wait_ld(r[0]);
-    reg_order(r[1]);
-    reg_order(r[2]);
-    reg_order(r[3]);
-    if (masked) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (kbase + 32 * c + i > lim) r[c][i] = __float_as_uint(-INFINITY);
+    for (int r = 0; r < 2; ++r) {
+        float e0, e1, e2, e3;
+        f2_unpack(acc_e[r][0], e0, e1);
+        f2_unpack(acc_e[r][1], e2, e3);
+        se[r] = (e0 + e1) + (e2 + e3);
+        sr[r] = acc_r[r][0] + acc_r[r][1];
     }
 }
 
+// On a tile that straddles the diagonal or the end of the keys, keys past a
+// row's last visible key become -inf.
+__device__ __forceinline__ void mask_tile(uint32_t (&s)[64], int key0, int lim_a, int lim_b) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int key = key0 + 8 * n + (k & 1);
+            if (key > ((k < 2) ? lim_a : lim_b)) s[4 * n + k] = __float_as_uint(-INFINITY);
+        }
+}
+
+// Per-thread softmax state of one query tile: running reference m (log2
+// units, the same in the four threads of a row) and this thread's partial
+// exact (l) and bf16-rounded (lr) row sums, for rows a and b.
+struct RowState {
+    float m[2], l[2], lr[2];
+};
+
+// One S tile through the softmax: S -> P (bf16, in place in tensor memory),
+// sums and reference updated, O rescaled when the reference moves.
 template <int D>
-__device__ void softmax_wg(int t, Bars* bars, uint32_t tmem, const PrefillParams& p,
-                           const WaitGuard& g) {
+__device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint32_t o_addr,
+                                             bool masked, int key0, int lim_a, int lim_b,
+                                             bool first, float scale_log2) {
+    uint32_t s[64];
+    tmem_ld_16x256b_x16(s_addr, s);
+    tmem_wait_ld64(s);
+    if (masked) mask_tile(s, key0, lim_a, lim_b);
+    // Fast path: weights against the running reference without a row
+    // maximum.  bf16 P and the fp32 sums and accumulators have fp32's
+    // exponent range, so weights far above 1 lose no relative precision; a
+    // partial sum above 2^62 (a row sum above 2^64) or one that is not finite
+    // means m must move, and the warp redoes the tile on the exact path.  A
+    // row's first tile always takes the exact path.
+    uint32_t pk[32];
+    float se[2], sr[2];
+    bool exact = first;
+    if (!first) {
+        if (masked)
+            tile_exp2<false>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+        else
+            tile_exp2<true>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+        exact = !(se[0] <= 0x1p62f) || !(se[1] <= 0x1p62f);
+    }
+    if (__any_sync(0xffffffffu, exact)) {
+        // Exact path: row maximum (this thread's 32 keys, then the four
+        // threads of the row), move m and rescale l, lr and O.
+        float mx[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float c0 = fmaxf(__uint_as_float(s[2 * r]), __uint_as_float(s[2 * r + 1]));
+            float c1 = fmaxf(__uint_as_float(s[4 + 2 * r]), __uint_as_float(s[4 + 2 * r + 1]));
+#pragma unroll
+            for (int n = 2; n < 16; n += 2) {
+                c0 = fmax3(c0, __uint_as_float(s[4 * n + 2 * r]), __uint_as_float(s[4 * n + 2 * r + 1]));
+                c1 = fmax3(c1, __uint_as_float(s[4 * n + 4 + 2 * r]),
+                           __uint_as_float(s[4 * n + 4 + 2 * r + 1]));
+            }
+            float v = fmaxf(c0, c1);
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+            mx[r] = v;
+        }
+        float alpha[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float m_new = fmaxf(st.m[r], mx[r] * scale_log2);
+            const float m_use = (m_new == -INFINITY) ? st.m[r] : m_new;
+            alpha[r] = (st.m[r] == -INFINITY) ? 0.0f : ex2_approx(st.m[r] - m_use);
+            st.l[r] *= alpha[r];
+            st.lr[r] *= alpha[r];
+            st.m[r] = m_use;
+        }
+        if (!first) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t ov[32];
+                tmem_ld_16x256b_x8(o_addr + 64 * c, ov);
+                tmem_wait_ld(ov);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[(i >> 1) & 1]);
+                tmem_st_16x256b_x8(o_addr + 64 * c, ov);
+            }
+        }
+        const float nma = (st.m[0] == -INFINITY) ? 0.0f : -st.m[0];
+        const float nmb = (st.m[1] == -INFINITY) ? 0.0f : -st.m[1];
+        if (masked)
+            tile_exp2<false>(s, scale_log2, nma, nmb, pk, se, sr);
+        else
+            tile_exp2<true>(s, scale_log2, nma, nmb, pk, se, sr);
+    }
+    // P overwrites the first 64 columns of the tile (keys 2j, 2j+1 in column j).
+    tmem_st_16x128b_x16(s_addr, pk);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        st.l[r] += se[r];
+        st.lr[r] += sr[r];
+    }
+}
+
+// Softmax warps 4-11: each 16-row slice of both query tiles belongs to one
+// warp (lane quarter warp % 4, half (warp - 4) / 4), so every tile is worked
+// on by two warps per SM sub-partition.  Per key tile the tiles are taken in
+// the order the MMA warp produces them (S0 before S1).
+template <int D>
+__device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
+                              const WaitGuard& g) {
     using C = Cfg<D>;
-    const int row_in_tile = threadIdx.x - 128 * (1 + t);  // = TMEM lane
     const int warp = threadIdx.x / 32;
-    const uint32_t lane_addr = tmem_lane_base(tmem, warp);
-    const uint32_t colS = C::col_s(t), colO = C::col_o(t);
+    const int lane = threadIdx.x % 32;
+    const int l0 = 32 * (warp & 3) + 16 * ((warp - 4) >> 2);  // first TMEM lane of this warp
+    const int ra = l0 + lane / 4;                              // rows a, a + 8 of a tile
+    const int kq = 2 * (lane & 3);                             // key offset inside a chunk
+    const uint32_t lanes = tmem + (static_cast<uint32_t>(l0) << 16);
     const int off = p.Tk - p.Tq;
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
 
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
         const int idx = snake_item(k, p.n_items);
         if (idx < 0) continue;
         const Item it = decode_item(idx, p);
-        const int n = it.n[t];
-        if (n == 0) continue;
-        const int r0 = it.qb * kItemRows + t * BM;
-        const int row = r0 + row_in_tile;
-        // Last visible key of this row and of the tile's first row.
-        const int lim = p.causal ? min(row + off, p.Tk - 1) : p.Tk - 1;
-        const int lim_first = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
-        float m = -INFINITY, l = 0.0f, lr = 0.0f;
-
-        for (int j = 0; j < n; ++j) {
-            // Warp-uniform outcome: tcgen05.ld below needs the whole warp.
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], s_cnt & 1, g, SITE_S_FULL)))
-                return;
-            ++s_cnt;
-            tc_fence_after_sync();
-            uint32_t r[4][32];
-            const int kbase = j * BN;
-            const bool masked = kbase + BN - 1 > lim_first;  // straddles the diagonal or Tk
-            load_scores(r, lane_addr + colS, masked, kbase, lim);
-            // Fast path: weights against the running reference m without a
-            // row maximum.  bf16 P and the fp32 sums and accumulators have
-            // fp32's exponent range, so weights far above 1 lose no relative
-            // precision; a tile whose exact weight sum exceeds 2^64 (or is not
-            // finite) means m must move, and it is redone on the exact path.
-            // The first tile of a row always takes the exact path.
-            float sum_e = 0.0f, sum_r = 0.0f;
-            bool exact = (m == -INFINITY);
-            if (!__any_sync(0xffffffffu, exact)) {
-                if (masked)
-                    row_exp2<false>(r, p.scale_log2, -m, sum_e, sum_r);
-                else
-                    row_exp2<true>(r, p.scale_log2, -m, sum_e, sum_r);
-                exact = !(sum_e <= 0x1p64f);
-                if (__any_sync(0xffffffffu, exact))  // S was packed in place: reload it
-                    load_scores(r, lane_addr + colS, masked, kbase, lim);
+        const int nkv = max(it.n[0], it.n[1]);
+        RowState st[2];
+        int lim_a[2], lim_b[2], lim_first[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const int r0 = it.qb * kItemRows + t * BM;
+            // Last visible key of rows a, b and of the tile's first row.
+            lim_a[t] = p.causal ? min(r0 + ra + off, p.Tk - 1) : p.Tk - 1;
+            lim_b[t] = p.causal ? min(r0 + ra + 8 + off, p.Tk - 1) : p.Tk - 1;
+            lim_first[t] = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
+            st[t].m[0] = st[t].m[1] = -INFINITY;
+            st[t].l[0] = st[t].l[1] = st[t].lr[0] = st[t].lr[1] = 0.0f;
+        }
+        for (int j = 0; j < nkv; ++j) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (j >= it.n[t]) continue;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], s_cnt[t] & 1, g, SITE_S_FULL)))
+                    return;
+                ++s_cnt[t];
+                tc_fence_after_sync();
+                const int kbase = j * BN;
+                softmax_tile<D>(st[t], lanes + C::col_s(t), lanes + C::col_o(t),
+                                kbase + BN - 1 > lim_first[t], kbase + kq, lim_a[t], lim_b[t],
+                                j == 0, p.scale_log2);
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(&bars->p_full[t]);
             }
-            if (__any_sync(0xffffffffu, exact)) {
-                // Exact path: row maximum (four independent 3-input max chains),
-                // move m to the running maximum and rescale l, lr and O.
-                float mc[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float a = fmaxf(__uint_as_float(r[c][0]), __uint_as_float(r[c][1]));
-#pragma unroll
-                    for (int i = 2; i < 32; i += 2)
-                        a = fmax3(a, __uint_as_float(r[c][i]), __uint_as_float(r[c][i + 1]));
-                    mc[c] = a;
-                }
-                const float mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
-                const float m_new = fmaxf(m, mx * p.scale_log2);
-                const float m_use = (m_new == -INFINITY) ? m : m_new;
-                const float alpha = (m == -INFINITY) ? 0.0f : ex2_approx(m - m_use);
-                l *= alpha;
-                lr *= alpha;
-                if (j > 0) {
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_addr + colO + 32 * c, ov);
-                        tmem_wait_ld(ov);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(lane_addr + colO + 32 * c, ov);
-                    }
-                }
-                m = m_use;
-                const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-                if (masked)
-                    row_exp2<false>(r, p.scale_log2, neg_m, sum_e, sum_r);
-                else
-                    row_exp2<true>(r, p.scale_log2, neg_m, sum_e, sum_r);
-            }
-            // Chunk c's 16 packed columns hold keys 32c .. 32c+31.
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_st16(lane_addr + colS + 16 * c, r[c]);
-            tmem_wait_st();
-            l += sum_e;
-            lr += sum_r;
-            tc_fence_before_sync();
-            mbar_arrive(&bars->p_full[t]);
         }
 
         // Epilogue: O = O_acc / lr -> bf16; lse = (m + log2 l) * ln 2.
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], o_cnt & 1, g, SITE_O_FULL)))
-            return;
-        ++o_cnt;
-        tc_fence_after_sync();
-        const float inv_l = 1.0f / lr;
-        const bool in_range = row < p.Tq;
-        uint16_t* orow = p.o + (static_cast<int64_t>(it.bh) * p.Tq + row) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(lane_addr + colO + 32 * c, ov);
-            tmem_wait_ld(ov);
-            uint32_t pk[16];
+        for (int t = 0; t < 2; ++t) {
+            if (it.n[t] == 0) continue;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_full[t], o_cnt[t] & 1, g, SITE_O_FULL)))
+                return;
+            ++o_cnt[t];
+            tc_fence_after_sync();
+            float l[2], lr[2];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
-                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
-            if (in_range) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            for (int r = 0; r < 2; ++r) {
+                l[r] = st[t].l[r] + __shfl_xor_sync(0xffffffffu, st[t].l[r], 1);
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+                lr[r] = st[t].lr[r] + __shfl_xor_sync(0xffffffffu, st[t].lr[r], 1);
+                lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
             }
+            const float inv[2] = {1.0f / lr[0], 1.0f / lr[1]};
+            const int r0 = it.qb * kItemRows + t * BM;
+            const int row[2] = {r0 + ra, r0 + ra + 8};
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t ov[32];
+                tmem_ld_16x256b_x8(lanes + C::col_o(t) + 64 * c, ov);
+                tmem_wait_ld(ov);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (row[r] >= p.Tq) continue;
+                    uint32_t* orow = reinterpret_cast<uint32_t*>(
+                        p.o + (static_cast<int64_t>(it.bh) * p.Tq + row[r]) * D + 64 * c + kq);
+#pragma unroll
+                    for (int n = 0; n < 8; ++n)
+                        orow[4 * n] = pack_bf16x2(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
+                                                  __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
+                }
+            }
+            if ((lane & 3) == 0 && p.lse != nullptr) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    if (row[r] < p.Tq)
+                        p.lse[static_cast<int64_t>(it.bh) * p.Tq + row[r]] =
+                            (st[t].m[r] + __log2f(l[r])) * kLn2;
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&bars->o_empty[t]);
         }
-        if (in_range && p.lse != nullptr)
-            p.lse[static_cast<int64_t>(it.bh) * p.Tq + row] = (m + __log2f(l)) * kLn2;
-        tc_fence_before_sync();
-        mbar_arrive(&bars->o_empty[t]);
     }
 }
 
@@ -577,9 +645,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->p_full[t], BM);
+            mbar_init(&bars->p_full[t], kSoftmaxThreads);
             mbar_init(&bars->o_full[t], 1);
-            mbar_init(&bars->o_empty[t], BM);
+            mbar_init(&bars->o_empty[t], kSoftmaxThreads);
         }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -611,7 +679,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
     } else {
         regs_increase<kSoftmaxRegs>();
-        softmax_wg<D>((warp - 4) / 4, bars, tmem, p, g);
+        softmax_group<D>(bars, tmem, p, g);
     }
 
     tc_fence_before_sync();
