@@ -161,30 +161,40 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return p + ((1024u - (s & 1023u)) & 1023u);
 }
 
+// The low word of a shared-memory descriptor holds the start address >> 4 in
+// its low 14 bits.  Shared memory ends below 256 KB, so adding a byte offset
+// >> 4 to the low word moves the start address without carrying into the
+// other fields; this keeps each K step of an MMA group at one integer add.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t off16) {
+    const uint32_t lo = static_cast<uint32_t>(d) + off16;
+    return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // S[tmem cols] = Q_tile . K_tile^T : M = 128, N = 128, K = D in steps of 16.
+// K step kk reads columns 16kk .. 16kk+15: 64-column box kk/4, 32 bytes
+// (kk%4) into each 128-byte row.  qd/kd: descriptors of the tiles' first box.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false);
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = static_cast<uint32_t>((kk / 4) * kBoxBytes + (kk % 4) * 32);
-        const uint64_t a = smem_desc_sw128(q_smem + off, 16, 1024);
-        const uint64_t b = smem_desc_sw128(k_smem + off, 16, 1024);
-        mma_bf16_ss(d_tmem, a, b, idesc, kk > 0 ? 1u : 0u);
+        const uint32_t off16 = static_cast<uint32_t>(((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4);
+        mma_bf16_ss(d_tmem, desc_advance(qd, off16), desc_advance(kd, off16), idesc,
+                    kk > 0 ? 1u : 0u);
     }
 }
 
 // O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
-// P is read from tensor memory (8 columns per 16 keys); V is MN-major.
+// P is read from tensor memory (8 columns per 16 keys); V is MN-major, K step
+// kk starts 16 key rows (2 KB) further.  vd: descriptor of the V tile.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd,
                                          bool accumulate) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true);
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t b = smem_desc_sw128(v_smem + kk * 16 * 128, kBoxBytes, 1024);
-        mma_bf16_ts(o_tmem, p_tmem + kk * 8, b, idesc, (accumulate || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < BN / 16; ++kk)
+        mma_bf16_ts(o_tmem, p_tmem + kk * 8, desc_advance(vd, kk * (16 * 128 >> 4)), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // Wait without recording a timeout (used only while draining after an abort).
@@ -287,9 +297,15 @@ template <int D>
 __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const PrefillParams& p,
                            const WaitGuard& g) {
     using C = Cfg<D>;
-    const uint32_t k_base = smem_u32(smem + C::kKOff);
-    const uint32_t v_base = smem_u32(smem + C::kVOff);
-    uint32_t kv_it = 0, q_it = 0;
+    constexpr uint32_t kTile16 = C::kTileBytes >> 4;  // one tile in descriptor units
+    // Descriptors of the first Q, K and V tiles; the others are kTile16 apart.
+    const uint64_t q_desc0 = smem_desc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
+    const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
+    const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + C::kVOff), kBoxBytes, 1024);
+    // Rolling ring positions: stage and phase parity of the next K and V tile
+    // and of the V tile of the previous key tile (read by PV1 one step late).
+    uint32_t ks = 0, kph = 0, vs = 0, vph = 0, pvs = 0, pvph = 0;
+    uint32_t q_it = 0;
     uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
 
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
@@ -298,48 +314,41 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
         const Item it = decode_item(idx, p);
         const int n0 = it.n[0], n1 = it.n[1];
         const int nkv = max(n0, n1);
-        const int qs = q_it % C::kQStages;
+        const uint32_t qs = q_it % C::kQStages;
         if (!warp_wait(&bars->q_full[qs], (q_it / C::kQStages) & 1, g, SITE_Q_FULL)) goto drain;
         ++q_it;
         tc_fence_after_sync();
-        const uint32_t q_base = smem_u32(smem + C::kQOff + qs * NQT * C::kTileBytes);
-        const uint32_t first = kv_it;
+        const uint64_t q_desc = desc_advance(q_desc0, qs * NQT * kTile16);
         for (int j = 0; j <= nkv; ++j) {
-            const uint32_t itj = first + j;
-            const int ks = itj % C::kKStages, vs = itj % C::kVStages;
-            const uint32_t kph = (itj / C::kKStages) & 1, vph = (itj / C::kVStages) & 1;
-            const uint32_t k_smem = k_base + ks * C::kTileBytes;
-            const uint32_t v_smem = v_base + vs * C::kTileBytes;
+            const uint64_t k_desc = desc_advance(k_desc0, ks * kTile16);
+            const uint64_t v_desc = desc_advance(v_desc0, vs * kTile16);
             if (j < nkv) {
                 if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
                 if (j < n0) {
-                    issue_qk<D>(tmem + C::col_s(0), q_base, k_smem);
+                    issue_qk<D>(tmem + C::col_s(0), q_desc, k_desc);
                     mma_commit(&bars->s_full[0]);
                 }
             }
             if (j >= 1 && j - 1 < n1) {  // PV1(j-1)
-                const uint32_t ip = itj - 1;
-                const int pvs = ip % C::kVStages;
                 if (!warp_wait(&bars->p_full[1], p_cnt[1] & 1, g, SITE_P_FULL)) goto drain;
                 ++p_cnt[1];
-                if (!warp_wait(&bars->v_full[pvs], (ip / C::kVStages) & 1, g, SITE_V_FULL))
-                    goto drain;
+                if (!warp_wait(&bars->v_full[pvs], pvph, g, SITE_V_FULL)) goto drain;
                 if (j - 1 == 0 && o_cnt[1] > 0 &&
                     !warp_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
                     goto drain;
                 tc_fence_after_sync();
                 issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
-                            v_base + pvs * C::kTileBytes, j - 1 > 0);
+                            desc_advance(v_desc0, pvs * kTile16), j - 1 > 0);
                 if (j - 1 == n1 - 1) {
                     mma_commit(&bars->o_full[1]);
                     ++o_cnt[1];
                 }
             }
-            if (j >= 1) mma_commit(&bars->v_empty[(itj - 1) % C::kVStages]);
+            if (j >= 1) mma_commit(&bars->v_empty[pvs]);
             if (j < nkv) {
                 if (j < n1) {
-                    issue_qk<D>(tmem + C::col_s(1), q_base + C::kTileBytes, k_smem);
+                    issue_qk<D>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc);
                     mma_commit(&bars->s_full[1]);
                 }
                 mma_commit(&bars->k_empty[ks]);
@@ -352,15 +361,19 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                         !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
-                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_smem, j > 0);
+                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > 0);
                     if (j == n0 - 1) {
                         mma_commit(&bars->o_full[0]);
                         ++o_cnt[0];
                     }
                 }
+                // Advance the rings: this key tile's V becomes the previous one.
+                pvs = vs;
+                pvph = vph;
+                if (++ks == static_cast<uint32_t>(C::kKStages)) { ks = 0; kph ^= 1u; }
+                if (++vs == static_cast<uint32_t>(C::kVStages)) { vs = 0; vph ^= 1u; }
             }
         }
-        kv_it = first + nkv;
     }
 drain:
     // Wait for every MMA issued so far before tensor memory is released.
@@ -740,7 +753,8 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
         if (warp_wait(&bars->q_full[0], 0, g, SITE_DIAG_LOAD)) {
             tc_fence_after_sync();
-            issue_qk<D>(tmem, smem_u32(sa), smem_u32(sb));
+            issue_qk<D>(tmem, smem_desc_sw128(smem_u32(sa), 16, 1024),
+                        smem_desc_sw128(smem_u32(sb), 16, 1024));
             mma_commit(&bars->s_full[0]);
         }
     }
@@ -777,7 +791,7 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncthreads();
     if (warp == 0 && __all_sync(0xffffffffu, ok && !bars->abort)) {
         tc_fence_after_sync();
-        issue_pv<D>(tmem + 128, tmem, smem_u32(sv), false);
+        issue_pv<D>(tmem + 128, tmem, smem_desc_sw128(smem_u32(sv), kBoxBytes, 1024), false);
         mma_commit(&bars->s_full[0]);
     }
     ok = ok && !bars->abort;
