@@ -176,12 +176,18 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t off16) {
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false);
+    constexpr int kSteps = D / 16;
+    uint64_t a[kSteps], b[kSteps];
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
+    for (int kk = 0; kk < kSteps; ++kk) {
         const uint32_t off16 = static_cast<uint32_t>(((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4);
-        mma_bf16_ss(d_tmem, desc_advance(qd, off16), desc_advance(kd, off16), idesc,
-                    kk > 0 ? 1u : 0u);
+        a[kk] = desc_advance(qd, off16);
+        b[kk] = desc_advance(kd, off16);
     }
+    if constexpr (kSteps == 8)
+        mma_bf16_ss_x8(d_tmem, a, b, idesc, 0u);
+    else
+        mma_bf16_ss_x4(d_tmem, a, b, idesc, 0u);
 }
 
 // O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
@@ -191,10 +197,14 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd,
                                          bool accumulate) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true);
+    uint32_t a[BN / 16];
+    uint64_t b[BN / 16];
 #pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk)
-        mma_bf16_ts(o_tmem, p_tmem + kk * 8, desc_advance(vd, kk * (16 * 128 >> 4)), idesc,
-                    (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < BN / 16; ++kk) {
+        a[kk] = p_tmem + kk * 8;
+        b[kk] = desc_advance(vd, kk * (16 * 128 >> 4));
+    }
+    mma_bf16_ts_x8(o_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // Wait without recording a timeout (used only while draining after an abort).

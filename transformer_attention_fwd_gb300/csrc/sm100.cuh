@@ -390,6 +390,69 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// A group of MMAs into one accumulator in one statement: one elect.sync for
+// the group; the first MMA accumulates only if `accumulate`, the others always.
+// SS form: A and B from shared memory (descriptors a[k], b[k]).
+__device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4],
+                                               const uint64_t (&b)[4], uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, pa, pt;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %10, 0;\n\t"
+        "setp.eq.b32 pt, %9, %9;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, pa;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, pt;\n\t}"
+        :: "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]),
+           "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+           "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8],
+                                               const uint64_t (&b)[8], uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, pa, pt;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %18, 0;\n\t"
+        "setp.eq.b32 pt, %17, %17;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, pa;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, pt;\n\t}"
+        :: "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+           "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+           "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// TS form: A from tensor memory (addresses a[k]), B from shared memory.
+__device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, const uint32_t (&a)[8],
+                                               const uint64_t (&b)[8], uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, pa, pt;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %18, 0;\n\t"
+        "setp.eq.b32 pt, %17, %17;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, pa;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, pt;\n\t}"
+        :: "r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+           "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+           "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive once on bar when all previously issued tcgen05 async operations of
 // the issuing lane have completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
