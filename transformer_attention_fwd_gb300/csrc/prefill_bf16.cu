@@ -174,7 +174,8 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t off16) {
 // K step kk reads columns 16kk .. 16kk+15: 64-column box kk/4, 32 bytes
 // (kk%4) into each 128-byte row.  qd/kd: descriptors of the tiles' first box.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd,
+                                         uint32_t leader) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false);
     constexpr int kSteps = D / 16;
     uint64_t a[kSteps], b[kSteps];
@@ -185,9 +186,9 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t 
         b[kk] = desc_advance(kd, off16);
     }
     if constexpr (kSteps == 8)
-        mma_bf16_ss_x8(d_tmem, a, b, idesc, 0u);
+        mma_bf16_ss_x8(d_tmem, a, b, idesc, 0u, leader);
     else
-        mma_bf16_ss_x4(d_tmem, a, b, idesc, 0u);
+        mma_bf16_ss_x4(d_tmem, a, b, idesc, 0u, leader);
 }
 
 // O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
@@ -195,7 +196,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t 
 // kk starts 16 key rows (2 KB) further.  vd: descriptor of the V tile.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd,
-                                         bool accumulate) {
+                                         bool accumulate, uint32_t leader) {
     constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true);
     uint32_t a[BN / 16];
     uint64_t b[BN / 16];
@@ -204,7 +205,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         a[kk] = p_tmem + kk * 8;
         b[kk] = desc_advance(vd, kk * (16 * 128 >> 4));
     }
-    mma_bf16_ts_x8(o_tmem, a, b, idesc, accumulate ? 1u : 0u);
+    mma_bf16_ts_x8(o_tmem, a, b, idesc, accumulate ? 1u : 0u, leader);
 }
 
 // Wait without recording a timeout (used only while draining after an abort).
@@ -317,6 +318,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
     uint32_t ks = 0, kph = 0, vs = 0, vph = 0, pvs = 0, pvph = 0;
     uint32_t q_it = 0;
     uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+    const uint32_t leader = elect_leader();
 
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
         const int idx = snake_item(k, p.n_items);
@@ -336,8 +338,8 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                 if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
                 if (j < n0) {
-                    issue_qk<D>(tmem + C::col_s(0), q_desc, k_desc);
-                    mma_commit(&bars->s_full[0]);
+                    issue_qk<D>(tmem + C::col_s(0), q_desc, k_desc, leader);
+                    mma_commit(&bars->s_full[0], leader);
                 }
             }
             if (j >= 1 && j - 1 < n1) {  // PV1(j-1)
@@ -349,20 +351,21 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                     goto drain;
                 tc_fence_after_sync();
                 issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
-                            desc_advance(v_desc0, pvs * kTile16), j - 1 > 0);
+                            desc_advance(v_desc0, pvs * kTile16), j - 1 > 0, leader);
                 if (j - 1 == n1 - 1) {
-                    mma_commit(&bars->o_full[1]);
+                    mma_commit(&bars->o_full[1], leader);
                     ++o_cnt[1];
                 }
             }
-            if (j >= 1) mma_commit(&bars->v_empty[pvs]);
+            if (j >= 1) mma_commit(&bars->v_empty[pvs], leader);
             if (j < nkv) {
                 if (j < n1) {
-                    issue_qk<D>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc);
-                    mma_commit(&bars->s_full[1]);
+                    issue_qk<D>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc,
+                                leader);
+                    mma_commit(&bars->s_full[1], leader);
                 }
-                mma_commit(&bars->k_empty[ks]);
-                if (j == nkv - 1) mma_commit(&bars->q_empty[qs]);
+                mma_commit(&bars->k_empty[ks], leader);
+                if (j == nkv - 1) mma_commit(&bars->q_empty[qs], leader);
                 if (j < n0) {  // PV0(j)
                     if (!warp_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
                     ++p_cnt[0];
@@ -371,9 +374,9 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                         !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
-                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > 0);
+                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > 0, leader);
                     if (j == n0 - 1) {
-                        mma_commit(&bars->o_full[0]);
+                        mma_commit(&bars->o_full[0], leader);
                         ++o_cnt[0];
                     }
                 }
@@ -387,7 +390,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
     }
 drain:
     // Wait for every MMA issued so far before tensor memory is released.
-    mma_commit(&bars->drain);
+    mma_commit(&bars->drain, leader);
     wait_quiet(&bars->drain, 0, kDrainLimitNs);
 }
 
@@ -761,11 +764,12 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
             }
         }
         __syncwarp();
+        const uint32_t leader = elect_leader();
         if (warp_wait(&bars->q_full[0], 0, g, SITE_DIAG_LOAD)) {
             tc_fence_after_sync();
             issue_qk<D>(tmem, smem_desc_sw128(smem_u32(sa), 16, 1024),
-                        smem_desc_sw128(smem_u32(sb), 16, 1024));
-            mma_commit(&bars->s_full[0]);
+                        smem_desc_sw128(smem_u32(sb), 16, 1024), leader);
+            mma_commit(&bars->s_full[0], leader);
         }
     }
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[0], 0, g, SITE_DIAG_MMA));
@@ -800,9 +804,11 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0 && __all_sync(0xffffffffu, ok && !bars->abort)) {
+        const uint32_t leader = elect_leader();
         tc_fence_after_sync();
-        issue_pv<D>(tmem + 128, tmem, smem_desc_sw128(smem_u32(sv), kBoxBytes, 1024), false);
-        mma_commit(&bars->s_full[0]);
+        issue_pv<D>(tmem + 128, tmem, smem_desc_sw128(smem_u32(sv), kBoxBytes, 1024), false,
+                    leader);
+        mma_commit(&bars->s_full[0], leader);
     }
     ok = ok && !bars->abort;
     if (__all_sync(0xffffffffu, ok && mbar_wait(&bars->s_full[0], 1, g, SITE_DIAG_MMA))) {
@@ -817,7 +823,7 @@ diag_mma_tile_kernel(const __grid_constant__ CUtensorMap tmA,
         }
     }
     if (warp == 0) {
-        mma_commit(&bars->drain);
+        mma_commit(&bars->drain, elect_leader());
         wait_quiet(&bars->drain, 0, kDrainLimitNs);
     }
     tc_fence_before_sync();

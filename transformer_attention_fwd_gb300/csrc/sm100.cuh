@@ -362,43 +362,34 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// The MMA and commit wrappers below are executed by all 32 lanes of a
-// converged warp; elect.sync picks the one lane that issues.  Keeping the
-// issuing warp converged lets the descriptors stay warp-uniform, which makes
-// each tcgen05.mma issue about a third cheaper than from a lone divergent
-// lane (measured: about 39 against 59 cycles per instruction).
+// MMA issue.  The wrappers below are executed by all 32 lanes of a converged
+// warp; `leader` (from elect_leader(), taken once) is nonzero in exactly one
+// lane, which issues.  Keeping the warp converged keeps the operands
+// warp-uniform, and predicating on a stored flag instead of electing per
+// instruction matters: elect.sync waits for the warp's queued MMAs to be
+// taken by the tensor pipe (measured: about 200 cycles behind a queued group
+// of eight), while setp does not.
 
-// D[tmem] (+)= A[smem] . B[smem].
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// Nonzero in exactly one lane of the (converged) calling warp.
+__device__ __forceinline__ uint32_t elect_leader() {
+    uint32_t r;
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
+        "{\n\t.reg .pred e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(r) :: "memory");
+    return r;
 }
 
-// D[tmem] (+)= A[tmem] . B[smem]; A is M x K with two bf16 per 32-bit column.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
-}
-
-// A group of MMAs into one accumulator in one statement: one elect.sync for
-// the group; the first MMA accumulates only if `accumulate`, the others always.
+// A group of MMAs into one accumulator in one statement; the first MMA
+// accumulates only if `accumulate`, the others always.
 // SS form: A and B from shared memory (descriptors a[k], b[k]).
 __device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, const uint64_t (&a)[4],
                                                const uint64_t (&b)[4], uint32_t idesc,
-                                               uint32_t accumulate) {
+                                               uint32_t accumulate, uint32_t leader) {
     asm volatile(
         "{\n\t.reg .pred e, pa, pt;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %11, 0;\n\t"
         "setp.ne.b32 pa, %10, 0;\n\t"
         "setp.eq.b32 pt, %9, %9;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, pa;\n\t"
@@ -407,15 +398,15 @@ __device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, const uint64_t (
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, pt;\n\t}"
         :: "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]),
            "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
-           "r"(idesc), "r"(accumulate) : "memory");
+           "r"(idesc), "r"(accumulate), "r"(leader) : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8],
                                                const uint64_t (&b)[8], uint32_t idesc,
-                                               uint32_t accumulate) {
+                                               uint32_t accumulate, uint32_t leader) {
     asm volatile(
         "{\n\t.reg .pred e, pa, pt;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %19, 0;\n\t"
         "setp.ne.b32 pa, %18, 0;\n\t"
         "setp.eq.b32 pt, %17, %17;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, pa;\n\t"
@@ -428,16 +419,16 @@ __device__ __forceinline__ void mma_bf16_ss_x8(uint32_t d_tmem, const uint64_t (
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, pt;\n\t}"
         :: "r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
            "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
-           "r"(idesc), "r"(accumulate) : "memory");
+           "r"(idesc), "r"(accumulate), "r"(leader) : "memory");
 }
 
 // TS form: A from tensor memory (addresses a[k]), B from shared memory.
 __device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, const uint32_t (&a)[8],
                                                const uint64_t (&b)[8], uint32_t idesc,
-                                               uint32_t accumulate) {
+                                               uint32_t accumulate, uint32_t leader) {
     asm volatile(
         "{\n\t.reg .pred e, pa, pt;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %19, 0;\n\t"
         "setp.ne.b32 pa, %18, 0;\n\t"
         "setp.eq.b32 pt, %17, %17;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, pa;\n\t"
@@ -450,17 +441,17 @@ __device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, const uint32_t (
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, pt;\n\t}"
         :: "r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
            "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
-           "r"(idesc), "r"(accumulate) : "memory");
+           "r"(idesc), "r"(accumulate), "r"(leader) : "memory");
 }
 
 // Arrive once on bar when all previously issued tcgen05 async operations of
-// the issuing lane have completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+// the leader lane have completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar, uint32_t leader) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 e, %1, 0;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-        :: "r"(smem_u32(bar)) : "memory");
+        :: "r"(smem_u32(bar)), "r"(leader) : "memory");
 }
 
 // ---------------------------------------------------------------------------
