@@ -88,8 +88,9 @@ static_assert(128 * kCtrlRegs + 256 * kSoftmaxRegs <= kThreads * 168, "register 
 // (i % kPolyEvery) == kPolyEvery - 1, i.e. one pair in kPolyEvery (0: none).
 // GB300's MUFU issues ex2 at twice the rate of earlier Blackwell parts and the
 // softmax warps are bound by instruction issue, not by MUFU, so moving work
-// to the FMA pipe does not pay: measured on the T=8192 causal workload, none
-// (1150 TFLOP/s) beat one pair in 16 (1112), in 8 (1093) and in 4 (1057).
+// to the FMA pipe does not pay: measured on the T=8192 causal workload with
+// the current softmax layout, none (1387 TFLOP/s) beat one chunk in 8 (1329),
+// in 4 (1188), in 3 (1204) and in 2 (1109).
 #ifndef ATTN_PREFILL_POLY_EVERY
 #define ATTN_PREFILL_POLY_EVERY 0
 #endif
