@@ -126,6 +126,62 @@ def attention_f64(q, k, v, causal: bool, scale: float | None = None,
     return _load().attention_f64(q, k, v, causal, scale, rows, nthreads)
 
 
+def decode_paged_f64(q, kv_cache, block_table, seq_lens, scale: float | None = None,
+                     nthreads: int | None = None):
+    """Float64 decode attention over a paged KV cache; returns ``(o, lse)``.
+
+    The cache is a pool of physical blocks of ``page_size`` tokens, each
+    holding the K and the V rows of those tokens for every KV head
+    ("第 11 章 · Attention 入门", 11.11, the KV-cache / VMM passage: a block
+    holds N tokens' K + V for all KV heads, and ``block_table[req][t/16]``
+    names the physical block of token t of request req).
+
+    q: [B, Hq, D] or [B, Hq, 1, D]; kv_cache: [num_blocks, 2, Hkv, page_size,
+    D] (index 0 = K, 1 = V); block_table: [B, max_pages] integers;
+    seq_lens: [B] keys of each request.  The decode query sees all of its
+    request's keys.  Request b's keys are gathered token by token, t ->
+    block ``block_table[b, t // page_size]``, row ``t % page_size``, and the
+    plain attention of the dense oracle is taken over them.  A request with
+    no keys gets O = 0 and lse = -inf (its softmax is over an empty set).
+    o: [B, Hq, D]; lse: [B, Hq].
+    """
+    q = _as_f32(q)
+    if q.ndim == 4:
+        if q.shape[2] != 1:
+            raise ValueError("paged decode takes one query row per head")
+        q = q[:, :, 0, :]
+    kv = _as_f32(kv_cache)
+    bt = np.asarray(block_table.cpu() if hasattr(block_table, "cpu") else block_table,
+                    dtype=np.int64)
+    sl = np.asarray(seq_lens.cpu() if hasattr(seq_lens, "cpu") else seq_lens, dtype=np.int64)
+    if kv.ndim != 5 or kv.shape[1] != 2:
+        raise ValueError("kv_cache must be [num_blocks, 2, Hkv, page_size, D]")
+    B, Hq, D = q.shape
+    nblk, _, Hkv, P, Dk = kv.shape
+    if Dk != D or bt.shape[0] != B or sl.shape[0] != B:
+        raise ValueError("shape mismatch")
+    o = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        L = int(sl[b])
+        if L < 0 or L > bt.shape[1] * P:
+            raise ValueError("sequence length outside the block table")
+        if L == 0:
+            continue
+        t = np.arange(L)
+        blk = bt[b, t // P]
+        if (blk < 0).any() or (blk >= nblk).any():
+            raise ValueError("block id out of range")
+        k = kv[blk, 0, :, t % P, :]  # [L, Hkv, D]
+        v = kv[blk, 1, :, t % P, :]
+        k = np.ascontiguousarray(k.transpose(1, 0, 2))[None]  # [1, Hkv, L, D]
+        v = np.ascontiguousarray(v.transpose(1, 0, 2))[None]
+        ob, lb = attention_f64(q[b][None, :, None, :], k, v, False, scale, None, nthreads)
+        o[b] = ob[0, :, 0, :]
+        lse[b] = lb[0, :, 0]
+    return o, lse
+
+
 def _as_f32(x) -> np.ndarray:
     if hasattr(x, "detach"):  # torch tensor
         x = x.detach().to("cpu")
