@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 METRIC = "attn fwd TFLOP/s (causal prefill) & decode KV GB/s, % of GB300 roofline"
 PRIMARY = "llama3_8b_prefill_bf16_b1_hq32_hkv8_t8192_d128_causal"
 DECODE = "gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128"
+PAGED_DECODE = "gqa_paged_decode_bf16_b64_hq32_hkv8_tk4096_d128_p16"
 GPT2 = "gpt2s_prefill_bf16_b8_h12_t1024_d64_causal"
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -374,6 +375,27 @@ def run_secondary(args, attn, peaks, flush):
                      "note": "step time includes the stream kernel and the fragment combine kernel"},
     }
     del q, k, v, o, lse
+    # The same decode against a paged cache (16-token blocks in a random order).
+    from transformer_attention_fwd_gb300.inputs import PAGED_WORKLOADS, make_paged_workload
+    pw = PAGED_WORKLOADS[PAGED_DECODE]
+    q, kv, bt, sl = (x.cuda() for x in make_paged_workload(pw, 0))
+    o = torch.empty_like(q)
+    lse = torch.empty((pw.B, pw.Hq), dtype=torch.float32, device="cuda")
+    fn = lambda: attn.attn_fwd_decode_paged(q, kv, bt, sl, out=o, lse=lse)  # noqa: E731
+    fn()
+    _, _, kernels = attn.last_launch_info()
+    times = time_steps(fn, steps, 5)
+    ms = sum(times) / steps
+    gbs = pw.io_bytes() / (ms * 1e-3) / 1e9
+    out["paged_decode"] = {
+        "workload": PAGED_DECODE, "value": round(gbs, 1), "unit": "GB/s",
+        "ms_per_step": round(ms, 5), "algorithmic_bytes": pw.io_bytes(),
+        "kernels_per_step": kernels,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 4), "traffic": None,
+                     "note": "step time includes the length prefix, stream and combine kernels"},
+    }
+    del q, kv, bt, sl, o, lse
     # GPT-2-small-shaped causal prefill, D = 64.
     w = WORKLOADS[GPT2]
     q, k, v = (x.cuda() for x in make_workload(w, 0))
@@ -449,7 +471,19 @@ def run_profile_case(args):
     from transformer_attention_fwd_gb300 import build as b
     b.build()
     from transformer_attention_fwd_gb300 import attn
-    from transformer_attention_fwd_gb300.inputs import WORKLOADS, make_workload
+    from transformer_attention_fwd_gb300.inputs import (PAGED_WORKLOADS, WORKLOADS,
+                                                        make_paged_workload, make_workload)
+    if args.profile_case in PAGED_WORKLOADS:
+        pw = PAGED_WORKLOADS[args.profile_case]
+        q, kv, bt, sl = (x.cuda() for x in make_paged_workload(pw, 0))
+        fn = lambda: attn.attn_fwd_decode_paged(q, kv, bt, sl)  # noqa: E731
+        times = time_steps(fn, args.steps, args.warmup)
+        if attn.device_status() != attn.ATTN_OK:
+            raise RuntimeError(attn.last_error())
+        ms = sum(times) / len(times)
+        print(json.dumps({"profile_case": pw.name, "ms_per_step": round(ms, 5),
+                          "gbs": round(pw.io_bytes() / (ms * 1e-3) / 1e9, 1)}), flush=True)
+        return 0
     w = WORKLOADS[args.profile_case]
     q, k, v = (x.cuda() for x in make_workload(w, 0))
     o = torch.empty_like(q)

@@ -53,7 +53,8 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2, /* valid request this build cannot run (e.g. D) */
     ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
     ATTN_ERR_NO_MEMORY = 4,   /* workspace allocation failed */
-    ATTN_ERR_TIMEOUT = 5      /* a kernel pipeline wait ran out of time */
+    ATTN_ERR_TIMEOUT = 5,     /* a kernel pipeline wait ran out of time */
+    ATTN_ERR_BAD_INPUT = 6    /* a kernel found a device-side index out of range */
 } attn_status;
 
 typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
@@ -143,10 +144,48 @@ attn_status attn_fwd_decode_noalloc(const void* q, const void* k, const void* v,
                                     cudaStream_t stream);
 
 /*
+ * attn_fwd_decode_paged -- decode (one query row per (b, hq)) against a paged
+ * KV cache ("第 11 章 · Attention 入门", 11.11, the KV-cache / VMM passage: the
+ * cache is a pool of physical blocks of `page_size` tokens, each holding the K
+ * and the V rows of its tokens for every KV head, and block_table[req][t / 16]
+ * names the block of token t of request req; 16 is that passage's page size,
+ * any page_size >= 1 is accepted here).
+ *   q, o:        [B, Hq, 1, D] bf16, 16-byte aligned.
+ *   kv_cache:    [num_blocks, 2, Hkv, page_size, D] bf16 (index 0 of the second
+ *                dimension = K, 1 = V), 16-byte aligned.
+ *   block_table: [B, max_pages_per_seq] int32, device; entry [b][p] is the
+ *                block holding tokens p*page_size .. p*page_size+page_size-1 of
+ *                request b.  Entries past a request's last page are not read.
+ *   seq_lens:    [B] int32, device; keys of each request, 0 .. max_pages_per_seq
+ *                * page_size.  The query sees all of its request's keys (no
+ *                mask).  A request with 0 keys gets O = 0 and lse = -inf.
+ *   lse:         [B, Hq] float32 or NULL.
+ * The arithmetic is that of attn_fwd_decode's automatic mode: all keys of all
+ * (request, KV head) units are laid end to end and cut into one equal slice
+ * per SM; cut units are merged with the block-merge rule.  Workspace (length
+ * prefix, slice geometry, per-SM partials) is allocated and freed on `stream`
+ * (stream-ordered); a failed allocation returns ATTN_ERR_NO_MEMORY.
+ * Device-side checks: a block id outside 0 .. num_blocks-1 or a length outside
+ * 0 .. max_pages_per_seq*page_size is never used to address memory (block 0
+ * is read, the length clamped); it sets a flag that attn_get_device_status
+ * reports as ATTN_ERR_BAD_INPUT, and the outputs of that call are undefined.
+ * Host-side argument errors as for attn_fwd (ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_UNSUPPORTED), before anything is launched.
+ */
+attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache,
+                                  const int* block_table, const int* seq_lens,
+                                  void* o, float* lse, int B, int Hq, int Hkv,
+                                  int D, int page_size, int max_pages_per_seq,
+                                  int num_blocks, float scale,
+                                  cudaStream_t stream);
+
+/*
  * attn_get_device_status -- synchronise `stream`, then read and clear the
  * device status word of the current device.  Returns ATTN_ERR_TIMEOUT when a
  * kernel gave up on a pipeline wait since the last call (its outputs are
- * then undefined), ATTN_ERR_CUDA when synchronising failed, else ATTN_OK.
+ * then undefined), ATTN_ERR_BAD_INPUT when a kernel met a device-side index
+ * outside its declared range (attn_fwd_decode_paged), ATTN_ERR_CUDA when
+ * synchronising failed, else ATTN_OK.
  */
 attn_status attn_get_device_status(cudaStream_t stream);
 

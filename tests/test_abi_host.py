@@ -28,8 +28,9 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_prefill", "attn_fwd_decode", "attn_get_device_status",
-            "attn_last_error", "attn_diag_mma_tile", "attn_diag_wait_timeout"} <= set(names)
+    assert {"attn_fwd", "attn_fwd_prefill", "attn_fwd_decode", "attn_fwd_decode_paged",
+            "attn_get_device_status", "attn_last_error", "attn_diag_mma_tile",
+            "attn_diag_wait_timeout"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared but not exported"
 
@@ -73,6 +74,30 @@ def test_decode_split_count_range(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 128, 128, 0.1, 300, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 128, 128, 0.1, -1, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 3, 128, 128, 0.1, 0, None) == 1
+
+
+@pytest.mark.parametrize("args,code,msg", [
+    # q, kv, block_table, seq_lens, o, lse, B, Hq, Hkv, D, page, max_pages, num_blocks, scale
+    ((0, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 8, 0.1), 1, "non-null"),
+    ((FAKE, FAKE, 0, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 8, 0.1), 1, "non-null"),
+    ((FAKE, FAKE + 8, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 8, 0.1), 1, "16-byte"),
+    ((FAKE, FAKE, FAKE + 2, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 8, 0.1), 1, "4-byte"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 3, 128, 16, 4, 8, 0.1), 1, "multiple"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 80, 16, 4, 8, 0.1), 2, "D=80"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 0, 4, 8, 0.1), 1, ">= 1"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 0, 8, 0.1), 1, ">= 1"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 0, 0.1), 1, ">= 1"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 16, 4, 8, -1.0), 1, "scale"),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 1 << 20, 1 << 12, 8, 0.1), 1, "2^31"),
+])
+def test_paged_decode_arguments_rejected_before_launch(lib, args, code, msg):
+    f = lib.attn_fwd_decode_paged
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+    f.restype = ctypes.c_int
+    lib.attn_last_error.restype = ctypes.c_char_p
+    assert f(*args, None) == code
+    assert msg in lib.attn_last_error().decode()
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

@@ -23,6 +23,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_NO_MEMORY = 4
 ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_BAD_INPUT = 6
 ATTN_F32 = 0
 ATTN_BF16 = 1
 
@@ -30,6 +31,7 @@ STATUS_NAMES = {
     ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
     ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED", ATTN_ERR_CUDA: "ATTN_ERR_CUDA",
     ATTN_ERR_NO_MEMORY: "ATTN_ERR_NO_MEMORY", ATTN_ERR_TIMEOUT: "ATTN_ERR_TIMEOUT",
+    ATTN_ERR_BAD_INPUT: "ATTN_ERR_BAD_INPUT",
 }
 
 
@@ -49,6 +51,7 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         "attn_fwd": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "attn_fwd_prefill": [P, P, P, P, P, I, I, I, I, I, I, I, F, P],
         "attn_fwd_decode": [P, P, P, P, P, I, I, I, I, I, F, I, P],
+        "attn_fwd_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P],
         "attn_get_device_status": [P],
         "attn_diag_mma_tile": [P, P, P, P, P, I, P],
         "attn_diag_wait_timeout": [LL, P],
@@ -168,9 +171,44 @@ def attn_fwd_decode(q, k, v, scale: float | None = None, num_splits: int = 0, ou
     return o, lse
 
 
+def attn_fwd_decode_paged(q, kv_cache, block_table, seq_lens, scale: float | None = None,
+                          out=None, lse=None, want_lse: bool = True, stream=None):
+    """Decode against a paged KV cache (``attn_fwd_decode_paged``).
+
+    q: [B, Hq, 1, D] bf16; kv_cache: [num_blocks, 2, Hkv, page_size, D] bf16
+    (0 = K, 1 = V); block_table: [B, max_pages] int32; seq_lens: [B] int32; all
+    CUDA tensors.  Returns ``(o [B, Hq, 1, D], lse [B, Hq] or None)``.
+    """
+    for name, t in (("q", q), ("kv_cache", kv_cache), ("block_table", block_table),
+                    ("seq_lens", seq_lens)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or q.shape[2] != 1 or q.dtype != torch.bfloat16:
+        raise ValueError("q must be bf16 [B, Hq, 1, D]")
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.dtype != torch.bfloat16:
+        raise ValueError("kv_cache must be bf16 [num_blocks, 2, Hkv, page_size, D]")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    B, Hq, _, D = q.shape
+    nblk, _, Hkv, page, Dk = kv_cache.shape
+    if Dk != D or block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B], with q's B and D")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib.attn_fwd_decode_paged(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                                     _ptr(o), _ptr(lse), B, Hq, Hkv, D, page,
+                                     block_table.shape[1], nblk, scale, _stream_handle(stream)))
+    return o, lse
+
+
 def device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status as an
-    attn_status code (ATTN_ERR_TIMEOUT if a kernel wait ran out of time)."""
+    attn_status code (ATTN_ERR_TIMEOUT if a kernel wait ran out of time,
+    ATTN_ERR_BAD_INPUT if a kernel met an out-of-range device-side index)."""
     return lib.attn_get_device_status(_stream_handle(stream))
 
 

@@ -348,6 +348,54 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     return run_prefill(q, k, v, o, lse, s, env);
 }
 
+attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache, const int* block_table,
+                                  const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                                  int D, int page_size, int max_pages_per_seq, int num_blocks,
+                                  float scale, cudaStream_t stream) {
+    if (!q || !kv_cache || !block_table || !seq_lens || !o)
+        return fail(ATTN_ERR_INVALID_ARG, "q, kv_cache, block_table, seq_lens and o must be non-null");
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(o, 16))
+        return fail(ATTN_ERR_INVALID_ARG, "q, kv_cache and o must be 16-byte aligned");
+    if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return fail(ATTN_ERR_INVALID_ARG, "block_table, seq_lens and lse must be 4-byte aligned");
+    if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || page_size < 1 || max_pages_per_seq < 1 ||
+        num_blocks < 1)
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "B, Hq, Hkv, D, page_size, max_pages_per_seq and num_blocks must be >= 1");
+    if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim D=%d not supported (64 or 128)", D);
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    if (!std::isfinite(scale) || !(scale > 0.0f))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and positive (got %g)", (double)scale);
+    if (static_cast<long long>(B) * Hq > 0x7fffffffLL ||
+        static_cast<long long>(B) * max_pages_per_seq > 0x7fffffffLL)
+        return fail(ATTN_ERR_INVALID_ARG, "B*Hq and B*max_pages_per_seq must fit in 31 bits");
+    if (static_cast<long long>(max_pages_per_seq) * page_size > 0x7fffffffLL - 1024)
+        return fail(ATTN_ERR_INVALID_ARG, "max_pages_per_seq*page_size must be below 2^31 - 1024");
+    LaunchEnv env;
+    attn_status st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    const PagedShape s{B, Hq, Hkv, D, page_size, max_pages_per_seq, num_blocks, scale};
+    const size_t bytes = decode_paged_workspace_bytes(s, env.num_sms);
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
+    if (e != cudaSuccess || ws == nullptr) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, "paged decode workspace of %zu bytes: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    int grid = 0, kernels = 0;
+    e = launch_decode_paged_bf16(static_cast<const uint16_t*>(q),
+                                 static_cast<const uint16_t*>(kv_cache),
+                                 reinterpret_cast<const int32_t*>(block_table),
+                                 reinterpret_cast<const int32_t*>(seq_lens),
+                                 static_cast<uint16_t*>(o), lse, ws, s, env, &grid, &kernels);
+    cudaError_t f = cudaFreeAsync(ws, env.stream);
+    if (e == cudaSuccess && f != cudaSuccess) e = f;
+    if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+    record_launch(grid, 0, kernels);
+    return ok();
+}
+
 attn_status attn_get_device_status(cudaStream_t stream) {
     LaunchEnv env;
     attn_status st = device_env(stream, &env);
@@ -362,9 +410,14 @@ attn_status attn_get_device_status(cudaStream_t stream) {
         e = cudaMemcpy(env.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
     }
-    if (word & 1u)
+    constexpr unsigned kTimeoutBit = 1u, kBadInputBit = 2u;  // as the kernels set them (sm100.cuh)
+    if (word & kTimeoutBit)
         return fail(ATTN_ERR_TIMEOUT, "a kernel pipeline wait timed out (site %u); outputs undefined",
                     (word >> 8) & 0xffu);
+    if (word & kBadInputBit)
+        return fail(ATTN_ERR_BAD_INPUT,
+                    "a block id or sequence length was out of range (a safe substitute was used); "
+                    "outputs undefined");
     return ok();
 }
 

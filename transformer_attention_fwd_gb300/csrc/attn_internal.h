@@ -57,6 +57,20 @@ cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, cons
                                       const LaunchEnv& env, int* grid_out, int* kernels_launched);
 size_t decode_workspace_bytes(const Shape& s, int splits);
 
+// Decode over a paged KV cache: kv [num_blocks, 2, Hkv, page, D], block_table
+// [B, max_pages], seq_lens [B] (device).  The workspace holds the length
+// prefix, the slice geometry and the fragment slots.
+struct PagedShape {
+    int B, Hq, Hkv, D;
+    int page, max_pages, num_blocks;
+    float scale;
+};
+size_t decode_paged_workspace_bytes(const PagedShape& s, int num_sms);
+cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     uint16_t* o, float* lse, void* ws, const PagedShape& s,
+                                     const LaunchEnv& env, int* grid_out, int* kernels_launched);
+
 // Diagnostics.
 cudaError_t launch_diag_mma_tile(const CUtensorMap& a, const CUtensorMap& b,
                                  const CUtensorMap& v, float* s_out, float* o_out, int D,

@@ -474,6 +474,17 @@ constexpr int kStreamStages = 5;
 
 enum : unsigned { SITE_DEC_FULL = 40, SITE_DEC_EMPTY, SITE_DEC_SEG };
 
+// Paged cache ("第 11 章 · Attention 入门", 11.11, the KV-cache / VMM passage:
+// physical blocks of `page` tokens hold the K and V rows of those tokens for
+// every KV head; block_table[req][t / page] names the block of token t).
+struct PagedParams {
+    const uint16_t* kv;          // [num_blocks, 2, Hkv, page, D], 0 = K, 1 = V
+    const int32_t* block_table;  // [B, max_pages]
+    const long long* cum;        // [B + 1] keys of requests 0..b-1 (prefix kernel)
+    const long long* geom;       // [2] total virtual keys, keys per CTA
+    int B, page, max_pages, num_blocks;
+};
+
 struct StreamParams {
     const uint16_t* q;
     const uint16_t* k;
@@ -487,6 +498,7 @@ struct StreamParams {
     float scale_log2;
     unsigned* status;
     unsigned long long limit_ns;
+    PagedParams pg;
 };
 
 struct StreamBars {
@@ -512,25 +524,115 @@ struct StreamLayout {
     static constexpr int kBytes = kBarOff + static_cast<int>(sizeof(StreamBars)) + 128;
 };
 
+// One unit (request b, KV head hkv, head chunk) fragment [k0, k1) of its L
+// keys; u numbers the units in (b, hkv, chunk) order.
 struct Segment {
     long long u;
-    int k0, k1;
+    int b, hkv, chunk;
+    int k0, k1, L;
 };
 
-// Next fragment [k0, k1) of unit u inside the virtual key range [v, v1).
-__device__ __forceinline__ bool next_segment(long long& v, long long v1, int Tk, Segment& sg) {
+// Next fragment inside the virtual key range [v, v1): every unit has Tk keys.
+__device__ __forceinline__ bool next_segment(long long& v, long long v1, const StreamParams& p,
+                                             Segment& sg) {
     if (v >= v1) return false;
+    const int Tk = p.Tk;
     sg.u = v / Tk;
+    sg.L = Tk;
     sg.k0 = static_cast<int>(v - sg.u * Tk);
     const long long rem = v1 - v;
     sg.k1 = static_cast<int>(rem < Tk - sg.k0 ? sg.k0 + rem : Tk);
+    const long long pair = sg.u / p.chunks;
+    sg.chunk = static_cast<int>(sg.u - pair * p.chunks);
+    sg.b = static_cast<int>(pair / p.Hkv);
+    sg.hkv = static_cast<int>(pair % p.Hkv);
     v += sg.k1 - sg.k0;
     return true;
 }
 
+// The same with per-request lengths: request b's units start at
+// cum[b] * (Hkv * chunks), each L_b = cum[b + 1] - cum[b] keys long.
+__device__ __forceinline__ bool next_segment_paged(long long& v, long long v1,
+                                                   const StreamParams& p, Segment& sg) {
+    if (v >= v1) return false;
+    const long long U = static_cast<long long>(p.Hkv) * p.chunks;
+    const long long* cum = p.pg.cum;
+    int lo = 0, hi = p.pg.B - 1;  // last request whose first unit starts at or before v
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] * U <= v) lo = mid; else hi = mid - 1;
+    }
+    const long long L = cum[lo + 1] - cum[lo];  // > 0: v lies inside request lo
+    const long long r = v - cum[lo] * U;
+    const long long w = r / L;
+    sg.b = lo;
+    sg.hkv = static_cast<int>(w / p.chunks);
+    sg.chunk = static_cast<int>(w - static_cast<long long>(sg.hkv) * p.chunks);
+    sg.u = static_cast<long long>(lo) * U + w;
+    sg.L = static_cast<int>(L);
+    sg.k0 = static_cast<int>(r - w * L);
+    const long long rem = v1 - v;
+    sg.k1 = static_cast<int>(rem < L - sg.k0 ? sg.k0 + rem : L);
+    v += sg.k1 - sg.k0;
+    return true;
+}
+
+// Block id of page `page` of request b, checked against the pool: an id
+// outside it is reported in the status word and block 0 is used instead, so
+// the copy stays inside the pool and the stage still receives the bytes its
+// barrier expects.
+__device__ __forceinline__ int paged_block_id(const StreamParams& p, int b, int page) {
+    int blk = p.pg.block_table[static_cast<int64_t>(b) * p.pg.max_pages + page];
+    if (blk < 0 || blk >= p.pg.num_blocks) {
+        atomicOr(p.status, ATTN_DEV_BAD_INPUT);
+        blk = 0;
+    }
+    return blk;
+}
+
+// Bulk copies of keys [kc, kc + n) of a paged unit into a ring stage, one
+// per run of rows inside one block; pages pg0 + r0 .. pg0 + r0 + cnt - 1 of
+// the chunk, whose block ids are ids[0 .. cnt-1] (cnt <= 8).
+template <int D>
+__device__ __forceinline__ void copy_paged_pages(uint8_t* stage, int half_bytes,
+                                                 const StreamParams& p, const Segment& sg, int kc,
+                                                 int n, int r0, int cnt, const int (&ids)[8],
+                                                 uint64_t* bar) {
+    const int P = p.pg.page;
+    const int64_t head_rows = static_cast<int64_t>(P) * D;  // one head of one block
+    const int64_t block_elems = 2 * static_cast<int64_t>(p.Hkv) * head_rows;
+    const int pg0 = kc / P;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (i >= cnt) break;
+        const int page = pg0 + r0 + i;
+        const int t = max(kc, page * P);
+        const int t1 = min(kc + n, page * P + P);
+        const uint16_t* kbase = p.pg.kv + static_cast<int64_t>(ids[i]) * block_elems +
+                                static_cast<int64_t>(sg.hkv) * head_rows +
+                                static_cast<int64_t>(t - page * P) * D;
+        const uint32_t bytes = static_cast<uint32_t>(t1 - t) * D * 2;
+        const int off = (t - kc) * D * 2;
+        bulk_load(stage + off, kbase, bytes, bar);
+        bulk_load(stage + half_bytes + off, kbase + static_cast<int64_t>(p.Hkv) * head_rows, bytes,
+                  bar);
+    }
+}
+
+// Block ids of pages first .. first + cnt - 1 of request b (cnt <= 8), as
+// independent loads.
+__device__ __forceinline__ void load_block_ids(const StreamParams& p, int b, int first, int cnt,
+                                               int (&ids)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ids[i] = (i < cnt) ? paged_block_id(p, b, first + i) : 0;
+}
+
 // Nine warps put three on one SM sub-partition, whose 16K registers cap a
 // thread at 168 (HC = 8 spills a little; splitting the heads would re-read K/V).
-template <int D, int HC>
+// kPaged: keys come from the paged cache, per-request lengths, and cut units
+// leave their fragments in per-CTA slots (first segment of the CTA: slot 0,
+// last: slot 1).
+template <int D, int HC, bool kPaged>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 decode_stream_kernel(const StreamParams p) {
     using L = StreamLayout<D, HC>;
@@ -559,17 +661,60 @@ decode_stream_kernel(const StreamParams p) {
     }
     __syncthreads();
     const WaitGuard g{p.status, &bars->abort, p.limit_ns};
-    const long long v_begin = static_cast<long long>(blockIdx.x) * p.per_cta;
-    const long long v_end = v_begin + p.per_cta < p.total ? v_begin + p.per_cta : p.total;
+    const long long total = kPaged ? p.pg.geom[0] : p.total;
+    const long long per_cta = kPaged ? p.pg.geom[1] : p.per_cta;
+    const long long v_begin = static_cast<long long>(blockIdx.x) * per_cta;
+    const long long v_end = v_begin + per_cta < total ? v_begin + per_cta : total;
+    auto next = [&](long long& vv, Segment& sg) {
+        return kPaged ? next_segment_paged(vv, v_end, p, sg) : next_segment(vv, v_end, p, sg);
+    };
 
-    if (warp == kStreamWarps) {
+    if (warp == kStreamWarps && kPaged) {
+        // Producer (paged): lane 0 alone, like the dense producer (warp-wide
+        // operations would wait for its bulk copies to be taken by the copy
+        // engine).  The block ids of a chunk's first 8 pages are loaded as
+        // independent loads before the stage wait.
+        if (lane == 0) {
+            uint32_t it = 0;
+            long long v = v_begin;
+            Segment sg;
+            while (next(v, sg)) {
+                for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
+                    const int n = min(CK, sg.k1 - kc);
+                    const int s = it % kStreamStages;
+                    const int pg0 = kc / p.pg.page;
+                    const int np = (kc + n - 1) / p.pg.page - pg0 + 1;
+                    int ids[8];
+                    load_block_ids(p, sg.b, pg0, min(8, np), ids);
+                    if (it >= (uint32_t)kStreamStages &&
+                        !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY))
+                        goto drain_paged;
+                    uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
+                    mbar_arrive_expect_tx(&bars->full[s], 2u * static_cast<uint32_t>(n) * D * 2);
+                    for (int r0 = 0; r0 < np; r0 += 8) {
+                        if (r0 > 0) load_block_ids(p, sg.b, pg0 + r0, min(8, np - r0), ids);
+                        copy_paged_pages<D>(stage, kHalf, p, sg, kc, n, r0, min(8, np - r0), ids,
+                                            &bars->full[s]);
+                    }
+                }
+            }
+            goto out_paged;
+        drain_paged:
+            for (uint32_t i = (it > (uint32_t)kStreamStages ? it - kStreamStages : 0); i < it; ++i) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&bars->full[i % kStreamStages], (i / kStreamStages) & 1))
+                    if (global_timer_ns() - t0 > 200000000ull) break;
+            }
+        out_paged:;
+        }
+    } else if (warp == kStreamWarps) {
         // Producer: bulk-copy every chunk of this CTA's slice into the ring.
         if (lane == 0) {
             uint32_t it = 0;
             long long v = v_begin;
             Segment sg;
-            while (next_segment(v, v_end, p.Tk, sg)) {
-                const long long pair = sg.u / p.chunks;
+            while (next(v, sg)) {
+                const long long pair = static_cast<long long>(sg.b) * p.Hkv + sg.hkv;
                 for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
                     const int n = min(CK, sg.k1 - kc);
                     const int s = it % kStreamStages;
@@ -577,9 +722,9 @@ decode_stream_kernel(const StreamParams p) {
                         !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY))
                         goto drain;
                     const uint32_t bytes = static_cast<uint32_t>(n) * D * 2;
-                    const int64_t row = pair * p.Tk + kc;
                     uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
                     mbar_arrive_expect_tx(&bars->full[s], 2 * bytes);
+                    const int64_t row = pair * p.Tk + kc;
                     bulk_load(stage, p.k + row * D, bytes, &bars->full[s]);
                     bulk_load(stage + kHalf, p.v + row * D, bytes, &bars->full[s]);
                 }
@@ -598,11 +743,9 @@ decode_stream_kernel(const StreamParams p) {
         uint32_t it = 0, nseg = 0;
         long long v = v_begin;
         Segment sg;
-        while (next_segment(v, v_end, p.Tk, sg)) {
-            const long long pair = sg.u / p.chunks;
-            const int chunk = static_cast<int>(sg.u - pair * p.chunks);
-            const int b = static_cast<int>(pair / p.Hkv), hkv = static_cast<int>(pair % p.Hkv);
-            const int hq0 = hkv * p.group + chunk * HC;
+        while (next(v, sg)) {
+            const int b = sg.b;
+            const int hq0 = sg.hkv * p.group + sg.chunk * HC;
             float qf[HC][8];
 #pragma unroll
             for (int h = 0; h < HC; ++h) {
@@ -752,8 +895,12 @@ decode_stream_kernel(const StreamParams p) {
             if (!__all_sync(0xffffffffu, mbar_wait(&bars->seg_in, nseg & 1, g, SITE_DEC_SEG)))
                 goto done;
             {
-                const bool whole = sg.k0 == 0 && sg.k1 == p.Tk;
-                const long long seg = static_cast<long long>(blockIdx.x) - (sg.u * p.Tk) / p.per_cta;
+                const bool whole = sg.k0 == 0 && sg.k1 == sg.L;
+                // Fragment slot: dense, by unit and slice; paged, by CTA.
+                const long long slot0 =
+                    kPaged ? (2LL * blockIdx.x + (nseg == 0 ? 0 : 1)) * HC
+                           : (sg.u * p.nseg_max +
+                              (static_cast<long long>(blockIdx.x) - (sg.u * p.Tk) / p.per_cta)) * HC;
                 for (int idx = threadIdx.x; idx < HC * D; idx += kStreamWarps * 32) {
                     const int h = idx / D, d = idx % D;
                     float M = -INFINITY;
@@ -774,7 +921,7 @@ decode_stream_kernel(const StreamParams p) {
                         p.o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
                         if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
                     } else {
-                        const int64_t slot = (sg.u * p.nseg_max + seg) * HC + h;
+                        const int64_t slot = slot0 + h;
                         p.ws_o[slot * D + d] = out;
                         if (d == 0) p.ws_lse[slot] = lse2;
                     }
@@ -820,7 +967,97 @@ decode_stream_combine_kernel(const StreamParams p, int hc) {
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
 }
 
-template <int D, int HC>
+// Paged mode: prefix of the clamped request lengths and the slice geometry
+// (one block).  A length outside 0 .. max_pages * page is reported in the
+// status word and clamped into that range.
+__global__ void __launch_bounds__(1024)
+paged_prefix_kernel(const int32_t* seq_lens, int B, int max_keys, long long units_per_req,
+                    int grid, long long* cum, long long* geom, unsigned* status) {
+    __shared__ long long warp_tot[32];
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (B + nt - 1) / nt;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    long long mine = 0;
+    for (int b = b0; b < b1; ++b) {
+        int L = seq_lens[b];
+        if (L < 0 || L > max_keys) {
+            atomicOr(status, ATTN_DEV_BAD_INPUT);
+            L = L < 0 ? 0 : max_keys;
+        }
+        mine += L;
+    }
+    // Exclusive scan of the per-thread sums: within warps, then across warps.
+    const int lane = tid & 31, warp = tid >> 5;
+    long long incl = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = lane < nt / 32 ? warp_tot[lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long run = incl - mine + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        cum[b] = run;
+        int L = seq_lens[b];
+        L = L < 0 ? 0 : (L > max_keys ? max_keys : L);
+        run += L;
+    }
+    if (tid == nt - 1) {
+        cum[B] = run;  // the last thread's range ends at B (or is empty and run is the total)
+        const long long total = run * units_per_req;
+        geom[0] = total;
+        geom[1] = total > 0 ? (total + grid - 1) / grid : 1;
+    }
+}
+
+// Paged mode: merge the fragments of cut units (CTA slots) and give requests
+// without keys O = 0, lse = -inf; units one CTA covered were written directly.
+template <int D>
+__global__ void __launch_bounds__(D)
+decode_paged_combine_kernel(const StreamParams p, int hc) {
+    const int row = blockIdx.x;
+    const int d = threadIdx.x;
+    const int b = row / p.Hq, hq = row - b * p.Hq;
+    const int hkv = hq / p.group, hl = hq - hkv * p.group;
+    const int chunk = hl / hc, h = hl - chunk * hc;
+    const long long L = p.pg.cum[b + 1] - p.pg.cum[b];
+    if (L == 0) {
+        p.o[static_cast<int64_t>(row) * D + d] = 0;
+        if (d == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
+        return;
+    }
+    const long long U = static_cast<long long>(p.Hkv) * p.chunks;
+    const long long start = p.pg.cum[b] * U + (static_cast<long long>(hkv) * p.chunks + chunk) * L;
+    const long long per = p.pg.geom[1];
+    const long long c0 = start / per, c1 = (start + L - 1) / per;
+    if (c0 == c1) return;
+    float M = -INFINITY;
+    for (long long c = c0; c <= c1; ++c) {
+        const long long slot = 2 * c + ((c == c0 && start != c0 * per) ? 1 : 0);
+        M = fmaxf(M, p.ws_lse[slot * hc + h]);
+    }
+    float Ls = 0.0f, acc = 0.0f;
+    for (long long c = c0; c <= c1; ++c) {
+        const long long slot = (2 * c + ((c == c0 && start != c0 * per) ? 1 : 0)) * hc + h;
+        const float w = ex2_approx(p.ws_lse[slot] - M);
+        Ls += w;
+        acc = fmaf(w, p.ws_o[slot * D + d], acc);
+    }
+    const uint32_t pk = pack_bf16x2(acc / Ls, 0.0f);
+    p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
+    if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
+}
+
+template <int D, int HC, bool kPaged = false>
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
     using L = StreamLayout<D, HC>;
     static bool attr_set[64] = {};
@@ -828,22 +1065,22 @@ cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, HC>,
+        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, HC, kPaged>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    decode_stream_kernel<D, HC><<<grid, kStreamThreads, L::kBytes, st>>>(p);
+    decode_stream_kernel<D, HC, kPaged><<<grid, kStreamThreads, L::kBytes, st>>>(p);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool kPaged = false>
 cudaError_t launch_stream_d(const StreamParams& p, int hc, int grid, cudaStream_t st) {
     switch (hc) {
-        case 8: return launch_stream<D, 8>(p, grid, st);
-        case 4: return launch_stream<D, 4>(p, grid, st);
-        case 2: return launch_stream<D, 2>(p, grid, st);
-        default: return launch_stream<D, 1>(p, grid, st);
+        case 8: return launch_stream<D, 8, kPaged>(p, grid, st);
+        case 4: return launch_stream<D, 4, kPaged>(p, grid, st);
+        case 2: return launch_stream<D, 2, kPaged>(p, grid, st);
+        default: return launch_stream<D, 1, kPaged>(p, grid, st);
     }
 }
 
@@ -871,6 +1108,58 @@ size_t decode_stream_workspace_bytes(const Shape& s, int num_sms) {
     const StreamGeom g = stream_geom(s, num_sms);
     const size_t slots = static_cast<size_t>(s.B) * s.Hq * g.nseg_max;
     return slots * s.D * sizeof(float) + slots * sizeof(float) + 256;
+}
+
+size_t decode_paged_workspace_bytes(const PagedShape& s, int num_sms) {
+    const int group = s.Hq / s.Hkv;
+    const int hc = heads_per_cta(group);
+    const size_t frag = 2ull * num_sms * hc;  // fragment slots
+    return 16ull * (s.B + 1 + 2) + frag * s.D * sizeof(float) + frag * sizeof(float) + 256;
+}
+
+cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     uint16_t* o, float* lse, void* ws, const PagedShape& s,
+                                     const LaunchEnv& env, int* grid_out, int* kernels_launched) {
+    const int group = s.Hq / s.Hkv;
+    const int hc = heads_per_cta(group);
+    const int grid = env.num_sms;
+    const size_t frag = 2ull * grid * hc;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    long long* cum = reinterpret_cast<long long*>(base);
+    long long* geom = cum + (s.B + 1);
+    float* ws_o = reinterpret_cast<float*>(base + 16ull * (s.B + 1 + 2));
+    float* ws_lse = ws_o + frag * s.D;
+
+    StreamParams p{};
+    p.q = q; p.k = nullptr; p.v = nullptr; p.o = o; p.lse = lse;
+    p.ws_o = ws_o; p.ws_lse = ws_lse;
+    p.Hq = s.Hq; p.Hkv = s.Hkv; p.Tk = 0; p.group = group; p.chunks = group / hc;
+    p.nseg_max = 0; p.total = 0; p.per_cta = 0;
+    p.scale_log2 = s.scale * 1.4426950408889634f;
+    p.status = env.status;
+    p.limit_ns = env.wait_limit_ns;
+    p.pg.kv = kv; p.pg.block_table = block_table; p.pg.cum = cum; p.pg.geom = geom;
+    p.pg.B = s.B; p.pg.page = s.page; p.pg.max_pages = s.max_pages; p.pg.num_blocks = s.num_blocks;
+
+    const long long units_per_req = static_cast<long long>(s.Hkv) * p.chunks;
+    paged_prefix_kernel<<<1, 1024, 0, env.stream>>>(seq_lens, s.B, s.max_pages * s.page,
+                                                    units_per_req, grid, cum, geom, env.status);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = (s.D == 64) ? launch_stream_d<64, true>(p, hc, grid, env.stream)
+                        : launch_stream_d<128, true>(p, hc, grid, env.stream);
+    if (e == cudaSuccess) {
+        const int rows = s.B * s.Hq;
+        if (s.D == 64)
+            decode_paged_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, hc);
+        else
+            decode_paged_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, hc);
+        e = cudaGetLastError();
+    }
+    if (grid_out) *grid_out = grid;
+    if (kernels_launched) *kernels_launched = 3;
+    return e;
 }
 
 cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,

@@ -16,6 +16,9 @@ namespace attn {
 
 // Device status word bits (read by attn_get_device_status).
 constexpr unsigned ATTN_DEV_TIMEOUT = 1u;
+// A kernel found an input index outside its declared range (a paged-cache
+// block id or sequence length) and used a safe substitute instead.
+constexpr unsigned ATTN_DEV_BAD_INPUT = 2u;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -99,3 +99,62 @@ def make_qkv(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, D: int,
 
 def make_workload(w: Workload, seed: int = 0):
     return make_qkv(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.D, w.dtype, seed)
+
+
+@dataclass(frozen=True)
+class PagedWorkload:
+    """Decode against a paged KV cache: B requests of `seq_len` keys each in
+    blocks of `page` tokens ("第 11 章 · Attention 入门", 11.11, the KV-cache /
+    VMM passage: 16-token blocks holding K and V for all KV heads)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    seq_len: int
+    D: int
+    page: int
+
+    def io_bytes(self) -> int:
+        """Algorithmic HBM bytes: every cached K/V row of the requests once, Q,
+        O (bf16) and lse (fp32); the block table and lengths are not counted."""
+        q = self.B * self.Hq * self.D * 2
+        kv = 2 * self.B * self.Hkv * self.seq_len * self.D * 2
+        return q + kv + q + self.B * self.Hq * 4
+
+
+PAGED_WORKLOADS = {
+    "gqa_paged_decode_bf16_b64_hq32_hkv8_tk4096_d128_p16":
+        PagedWorkload("gqa_paged_decode_bf16_b64_hq32_hkv8_tk4096_d128_p16", 64, 32, 8, 4096, 128, 16),
+}
+
+
+def make_paged(B: int, Hq: int, Hkv: int, D: int, page: int, seq_lens, seed: int = 0,
+               spare_blocks: int = 3, max_pages: int | None = None):
+    """Draw a paged-cache decode problem on the CPU.
+
+    q [B, Hq, 1, D] and the block pool kv [num_blocks, 2, Hkv, page, D] are iid
+    N(0, 1) rounded to bf16; the pool has the blocks the requests need plus
+    `spare_blocks` unreferenced ones.  Request b's pages get distinct blocks in
+    a seeded random order; block-table entries past a request's last page are
+    -1 (never valid).  Returns (q, kv, block_table int32 [B, max_pages],
+    seq_lens int32 [B]).
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    lens = [int(x) for x in seq_lens]
+    pages = [-(-L // page) for L in lens]
+    if max_pages is None:
+        max_pages = max(1, max(pages))
+    nblk = sum(pages) + spare_blocks
+    q = torch.randn(B, Hq, 1, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.randn(nblk, 2, Hkv, page, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    perm = torch.randperm(nblk, generator=g)
+    table = torch.full((B, max_pages), -1, dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        table[b, :pages[b]] = perm[nxt:nxt + pages[b]].to(torch.int32)
+        nxt += pages[b]
+    return q, kv, table, torch.tensor(lens, dtype=torch.int32)
+
+
+def make_paged_workload(w: PagedWorkload, seed: int = 0):
+    return make_paged(w.B, w.Hq, w.Hkv, w.D, w.page, [w.seq_len] * w.B, seed)
