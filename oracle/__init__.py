@@ -49,12 +49,12 @@ class OracleLib:
 
     def __init__(self, path: str):
         lib = ctypes.CDLL(path)
-        fn = lib.attn_oracle_f64
+        fn = lib.attn_oracle_f64_window
         fn.restype = ctypes.c_int
         fn.argtypes = [
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int,
         ]
@@ -62,7 +62,7 @@ class OracleLib:
         self.path = path
 
     def attention_f64(self, q, k, v, causal: bool, scale: float | None = None,
-                      rows=None, nthreads: int | None = None):
+                      rows=None, nthreads: int | None = None, window: int = 0):
         """Return ``(o, lse)`` in float64.
 
         q: [B, Hq, Tq, D]; k, v: [B, Hkv, Tk, D] (numpy or CPU torch, any
@@ -72,7 +72,9 @@ class OracleLib:
         ``(b*Hq + h)*Tq + i``; then ``o`` is [len(rows), D] and ``lse`` is
         [len(rows)].  Otherwise ``o`` is [B, Hq, Tq, D] and ``lse`` is
         [B, Hq, Tq].  ``lse`` is the natural-log log-sum-exp of the scaled,
-        masked scores.
+        masked scores.  ``window`` > 0 (causal only) keeps, for each row, only
+        the most recent ``window`` keys up to its causal limit ("第 11 章 ·
+        Attention 入门" §11.8.4, Sliding Window Attention).
         """
         q = _as_f32(q)
         k = _as_f32(k)
@@ -95,9 +97,9 @@ class OracleLib:
             o = np.empty((B, Hq, Tq, D), dtype=np.float64)
             lse = np.empty((B, Hq, Tq), dtype=np.float64)
             rows_ptr, nrows = None, 0
-        rc = self._lib.attn_oracle_f64(
+        rc = self._lib.attn_oracle_f64_window(
             q.ctypes.data, k.ctypes.data, v.ctypes.data, B, Hq, Hkv, Tq, Tk, D,
-            1 if causal else 0, float(scale), rows_ptr, nrows, o.ctypes.data,
+            1 if causal else 0, int(window), float(scale), rows_ptr, nrows, o.ctypes.data,
             lse.ctypes.data, int(nthreads or default_threads()))
         if rc != 0:
             raise ValueError(f"attn_oracle_f64 failed with code {rc}")
@@ -121,9 +123,9 @@ def default_threads() -> int:
 
 
 def attention_f64(q, k, v, causal: bool, scale: float | None = None,
-                  rows=None, nthreads: int | None = None):
+                  rows=None, nthreads: int | None = None, window: int = 0):
     """Float64 attention of the built oracle; see ``OracleLib.attention_f64``."""
-    return _load().attention_f64(q, k, v, causal, scale, rows, nthreads)
+    return _load().attention_f64(q, k, v, causal, scale, rows, nthreads, window)
 
 
 def decode_paged_f64(q, kv_cache, block_table, seq_lens, scale: float | None = None,

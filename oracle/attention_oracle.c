@@ -17,6 +17,10 @@
  *       "Self-Attention机制深入理解" §10.2, the 4x4 mask example).  The
  *       offset Tk - Tq aligns the last query with the last key; for Tq == Tk
  *       it is the page's lower-triangular mask.
+ *   Sliding window (optional, with the causal mask).  With window W > 0 the
+ *       row also drops keys more than W - 1 positions before its own, so it
+ *       sees keys i + (Tk - Tq) - W + 1 .. i + (Tk - Tq): "only the most recent
+ *       W tokens" ("Attention 入门" §11.8.4, Sliding Window Attention).
  *   Stage 2, safe softmax with the row maximum subtracted
  *       ("Self-Attention机制深入理解" §7.2):
  *       m = max_j s_j,  Z = sum_j exp(s_j - m),  p_j = exp(s_j - m) / Z.
@@ -42,7 +46,7 @@
 
 typedef struct {
     const float *q, *k, *v;
-    int B, Hq, Hkv, Tq, Tk, D, causal;
+    int B, Hq, Hkv, Tq, Tk, D, causal, window;
     double scale;
     const int64_t *rows; /* NULL: every row, in [B, Hq, Tq] order */
     int64_t nrows;
@@ -67,16 +71,20 @@ static void oracle_row(const oracle_job *job, int64_t flat, double *s,
     const float *kh = job->k + (b * job->Hkv + hkv) * (int64_t)Tk * D;
     const float *vh = job->v + (b * job->Hkv + hkv) * (int64_t)Tk * D;
 
-    /* visible keys: 0 .. n_vis-1 */
-    int64_t n_vis = Tk;
+    /* visible keys: j0 .. n_vis-1 */
+    int64_t n_vis = Tk, j0 = 0;
     if (job->causal) {
         int64_t last = i + (int64_t)(Tk - Tq);
         n_vis = last + 1 < Tk ? last + 1 : Tk;
         if (n_vis < 0) n_vis = 0;
+        if (job->window > 0) {
+            int64_t first = last - (int64_t)job->window + 1;
+            j0 = first > 0 ? first : 0;
+        }
     }
 
     /* Stage 1: scaled scores of the visible keys. */
-    for (int64_t j = 0; j < n_vis; ++j) {
+    for (int64_t j = j0; j < n_vis; ++j) {
         double acc = 0.0;
         for (int d = 0; d < D; ++d)
             acc += (double)qrow[d] * (double)kh[j * D + d];
@@ -85,23 +93,23 @@ static void oracle_row(const oracle_job *job, int64_t flat, double *s,
 
     /* Stage 2: softmax with the row maximum subtracted. */
     double m = -INFINITY;
-    for (int64_t j = 0; j < n_vis; ++j)
+    for (int64_t j = j0; j < n_vis; ++j)
         if (s[j] > m) m = s[j];
     double z = 0.0;
-    for (int64_t j = 0; j < n_vis; ++j) {
+    for (int64_t j = j0; j < n_vis; ++j) {
         s[j] = exp(s[j] - m);
         z += s[j];
     }
-    for (int64_t j = 0; j < n_vis; ++j) s[j] /= z;
+    for (int64_t j = j0; j < n_vis; ++j) s[j] /= z;
 
     /* Stage 3: o = P V over the visible keys. */
     for (int d = 0; d < D; ++d) o_out[d] = 0.0;
-    for (int64_t j = 0; j < n_vis; ++j) {
+    for (int64_t j = j0; j < n_vis; ++j) {
         const double p = s[j];
         const float *vr = vh + j * D;
         for (int d = 0; d < D; ++d) o_out[d] += p * (double)vr[d];
     }
-    *lse_out = n_vis > 0 ? m + log(z) : -INFINITY;
+    *lse_out = n_vis > j0 ? m + log(z) : -INFINITY;
 }
 
 static void *oracle_worker(void *arg)
@@ -122,6 +130,15 @@ static void *oracle_worker(void *arg)
 }
 
 /*
+ * attn_oracle_f64_window: attn_oracle_f64 with a sliding window of `window`
+ * keys (0: none; needs causal != 0).
+ */
+int attn_oracle_f64_window(const float *q, const float *k, const float *v, int B,
+                           int Hq, int Hkv, int Tq, int Tk, int D, int causal,
+                           int window, double scale, const int64_t *rows,
+                           int64_t nrows, double *o, double *lse, int nthreads);
+
+/*
  * attn_oracle_f64: compute attention rows in float64.
  *   rows == NULL: all B*Hq*Tq rows; o is [B,Hq,Tq,D], lse is [B,Hq,Tq].
  *   rows != NULL: nrows flat row indices (b*Hq + hq)*Tq + i; o is [nrows,D],
@@ -134,7 +151,17 @@ int attn_oracle_f64(const float *q, const float *k, const float *v, int B,
                     double scale, const int64_t *rows, int64_t nrows,
                     double *o, double *lse, int nthreads)
 {
+    return attn_oracle_f64_window(q, k, v, B, Hq, Hkv, Tq, Tk, D, causal, 0, scale,
+                                  rows, nrows, o, lse, nthreads);
+}
+
+int attn_oracle_f64_window(const float *q, const float *k, const float *v, int B,
+                           int Hq, int Hkv, int Tq, int Tk, int D, int causal,
+                           int window, double scale, const int64_t *rows,
+                           int64_t nrows, double *o, double *lse, int nthreads)
+{
     if (!q || !k || !v || !o || !lse) return 1;
+    if (window < 0 || (window > 0 && !causal)) return 1;
     if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || D < 1) return 1;
     if (Hq % Hkv != 0) return 1;
     const int64_t total = (int64_t)B * Hq * Tq;
@@ -155,7 +182,7 @@ int attn_oracle_f64(const float *q, const float *k, const float *v, int B,
         oracle_job *j = &jobs[t];
         j->q = q; j->k = k; j->v = v;
         j->B = B; j->Hq = Hq; j->Hkv = Hkv; j->Tq = Tq; j->Tk = Tk; j->D = D;
-        j->causal = causal; j->scale = scale;
+        j->causal = causal; j->window = window; j->scale = scale;
         j->rows = rows; j->nrows = nrows; j->o = o; j->lse = lse;
         j->begin = nrows * t / nthreads;
         j->end = nrows * (t + 1) / nthreads;

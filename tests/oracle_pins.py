@@ -307,4 +307,61 @@ def pin_brute_force_tiny(attention):
                 assert abs(lse[0, h, i] - math.log(z)) <= 1e-12
 
 
+def pin_window_brute_force_tiny(attention):
+    """Sliding window ("第 11 章 · Attention 入门" §11.8.4: only the most recent
+    W tokens), literal definition on tiny inputs: row i sees keys
+    i + Tk - Tq - W + 1 .. i + Tk - Tq (Tq < Tk, so the offset matters)."""
+    B, Hq, Hkv, Tq, Tk, D = 1, 2, 1, 4, 7, 3
+    q, k, v = _qkv(B, Hq, Hkv, Tq, Tk, D, seed=54)
+    for W in (1, 2, 3, 5):
+        o, lse = attention(q, k, v, True, window=W)
+        for h in range(Hq):
+            for i in range(Tq):
+                a = i + Tk - Tq
+                vis = [j for j in range(Tk) if a - W < j <= a]
+                sc = {j: sum(float(q[0, h, i, d]) * float(k[0, 0, j, d])
+                             for d in range(D)) / math.sqrt(D) for j in vis}
+                z = sum(math.exp(sc[j]) for j in vis)
+                for d in range(D):
+                    want = sum(math.exp(sc[j]) / z * float(v[0, 0, j, d]) for j in vis)
+                    assert abs(o[0, h, i, d] - want) <= 1e-12
+                assert abs(lse[0, h, i] - math.log(z)) <= 1e-12
+
+
+def pin_window_of_one_returns_own_value(attention):
+    """W = 1: each row sees only the key at its own position, so O_i is that
+    key's value row and lse_i its scaled score."""
+    q, k, v = _qkv(2, 4, 2, 5, 9, 8, seed=55)
+    o, lse = attention(q, k, v, True, window=1)
+    kx, vx = _expand_kv(k, 4), _expand_kv(v, 4)
+    for i in range(5):
+        j = i + 4
+        assert np.array_equal(o[:, :, i], vx[:, :, j].astype(np.float64))
+        s = (q[:, :, i].astype(np.float64) * kx[:, :, j].astype(np.float64)).sum(-1) / math.sqrt(8)
+        assert np.abs(lse[:, :, i] - s).max() <= 1e-12
+
+
+def pin_window_covering_every_key_is_causal(attention):
+    q, k, v = _qkv(1, 2, 2, 6, 10, 4, seed=56)
+    o, lse = attention(q, k, v, True)
+    for W in (10, 11, 1000):
+        o2, lse2 = attention(q, k, v, True, window=W)
+        assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def pin_window_q_zero_gives_window_mean(attention):
+    """Q = 0: equal weights over the window, O_i = mean of its value rows,
+    lse_i = ln(number of keys in the window)."""
+    _, k, v = _qkv(1, 2, 1, 6, 11, 4, seed=57)
+    q = np.zeros((1, 2, 6, 4), np.float32)
+    W = 4
+    o, lse = attention(q, k, v, True, window=W)
+    for i in range(6):
+        a = i + 5
+        j0 = max(0, a - W + 1)
+        want = v[0, 0, j0:a + 1].astype(np.float64).mean(0)
+        assert np.abs(o[0, :, i] - want).max() <= 1e-12
+        assert np.abs(lse[0, :, i] - math.log(a + 1 - j0)).max() <= 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -18,11 +18,20 @@ MUTANTS = [
     ("mask_tq_aligned", "int64_t last = i + (int64_t)(Tk - Tq);", "int64_t last = i;"),
     ("scale_dropped", "s[j] = job->scale * acc;", "s[j] = acc;"),
     ("scale_squared", "s[j] = job->scale * acc;", "s[j] = job->scale * job->scale * acc;"),
-    ("lse_without_max", "*lse_out = n_vis > 0 ? m + log(z)", "*lse_out = n_vis > 0 ? log(z)"),
+    ("lse_without_max", "*lse_out = n_vis > j0 ? m + log(z)", "*lse_out = n_vis > j0 ? log(z)"),
+    ("window_one_key_short", "int64_t first = last - (int64_t)job->window + 1;",
+     "int64_t first = last - (int64_t)job->window + 2;"),
+    ("window_one_key_long", "int64_t first = last - (int64_t)job->window + 1;",
+     "int64_t first = last - (int64_t)job->window;"),
+    ("window_ignored", "if (job->window > 0) {", "if (0) {"),
+    ("window_from_row_index", "int64_t first = last - (int64_t)job->window + 1;",
+     "int64_t first = i - (int64_t)job->window + 1;"),
+    ("window_sum_from_zero", "for (int64_t j = j0; j < n_vis; ++j) {\n        s[j] = exp(s[j] - m);",
+     "for (int64_t j = 0; j < n_vis; ++j) {\n        s[j] = exp(s[j] - m);"),
     ("scores_use_v", "acc += (double)qrow[d] * (double)kh[j * D + d];",
      "acc += (double)qrow[d] * (double)vh[j * D + d];"),
     ("gqa_modulo_map", "const int64_t hkv = hq / group;", "const int64_t hkv = hq % job->Hkv;"),
-    ("softmax_not_normalised", "for (int64_t j = 0; j < n_vis; ++j) s[j] /= z;", ""),
+    ("softmax_not_normalised", "for (int64_t j = j0; j < n_vis; ++j) s[j] /= z;", ""),
     ("o_transposed_index", "o_out[d] += p * (double)vr[d];", "o_out[d] += p * (double)vh[d * D + j % D];"),
 ]
 
