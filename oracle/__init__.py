@@ -184,6 +184,59 @@ def decode_paged_f64(q, kv_cache, block_table, seq_lens, scale: float | None = N
     return o, lse
 
 
+def attention_varlen_f64(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool,
+                         scale: float | None = None, window: int = 0,
+                         seqs=None, nthreads: int | None = None):
+    """Float64 attention over sequences packed along the token axis; returns
+    ``(o, lse)``.
+
+    q: [total_q, Hq, D]; k, v: [total_k, Hkv, D] (the (T, H, D) layout of
+    "第 11 章 · Attention 入门", 11.11).  Sequence b owns query rows
+    ``cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1`` and key rows
+    ``cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1``; it is the plain attention of
+    the dense oracle over those rows alone, with the causal mask (and
+    ``window``) aligned to the end of its keys as in the dense oracle.  A
+    sequence with query rows but no keys gets O = 0 and lse = -inf (its
+    softmax is over an empty set).  ``seqs``: optional sequence indices to
+    compute; the others stay O = 0, lse = NaN.
+    o: [total_q, Hq, D]; lse: [Hq, total_q].
+    """
+    q, k, v = _as_f32(q), _as_f32(k), _as_f32(v)
+    cq = np.asarray(cu_seqlens_q.cpu() if hasattr(cu_seqlens_q, "cpu") else cu_seqlens_q,
+                    dtype=np.int64)
+    ck = np.asarray(cu_seqlens_k.cpu() if hasattr(cu_seqlens_k, "cpu") else cu_seqlens_k,
+                    dtype=np.int64)
+    if q.ndim != 3 or k.ndim != 3 or k.shape != v.shape or q.shape[2] != k.shape[2]:
+        raise ValueError("q must be [total_q, Hq, D] and k, v [total_k, Hkv, D]")
+    if cq.ndim != 1 or cq.shape != ck.shape or cq.shape[0] < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be [B + 1]")
+    TQ, Hq, D = q.shape
+    TK, Hkv, _ = k.shape
+    B = cq.shape[0] - 1
+    if (np.diff(cq) < 0).any() or cq[0] < 0 or cq[-1] > TQ:
+        raise ValueError("cu_seqlens_q is not a non-decreasing offset list inside q")
+    if (np.diff(ck) < 0).any() or ck[0] < 0 or ck[-1] > TK:
+        raise ValueError("cu_seqlens_k is not a non-decreasing offset list inside k")
+    o = np.zeros((TQ, Hq, D), dtype=np.float64)
+    lse = np.full((Hq, TQ), np.nan, dtype=np.float64)
+    for b in (range(B) if seqs is None else seqs):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            lse[:, q0:q1] = -np.inf
+            continue
+        if causal and q1 - q0 > k1 - k0:
+            raise ValueError("causal sequence with more queries than keys")
+        qb = np.ascontiguousarray(q[q0:q1].transpose(1, 0, 2))[None]  # [1, Hq, Tq, D]
+        kb = np.ascontiguousarray(k[k0:k1].transpose(1, 0, 2))[None]  # [1, Hkv, Tk, D]
+        vb = np.ascontiguousarray(v[k0:k1].transpose(1, 0, 2))[None]
+        ob, lb = attention_f64(qb, kb, vb, causal, scale, None, nthreads, window)
+        o[q0:q1] = ob[0].transpose(1, 0, 2)
+        lse[:, q0:q1] = lb[0]
+    return o, lse
+
+
 def _as_f32(x) -> np.ndarray:
     if hasattr(x, "detach"):  # torch tensor
         x = x.detach().to("cpu")
