@@ -3,12 +3,15 @@
 
 One step = one causal GQA prefill forward of the Llama-3-8B-shaped workload
 (B=1, Hq=32, Hkv=8, T=8192, D=128, bf16 I/O), through libattn.so's C ABI on
-inputs already resident in HBM.  The same run also times the split-KV decode
-workload (B=64, Hq=32, Hkv=8, Tk=4096, D=128) and the GPT-2-small-shaped
-prefill (B=8, H=12, T=1024, D=64) and reports them under "secondary".
+inputs already resident in HBM.  The same run also times, under "secondary":
+the stream-K decode (B=64, Hq=32, Hkv=8, Tk=4096, D=128) on a dense and on a
+paged cache, the GPT-2-small-shaped prefill (B=8, H=12, T=1024, D=64), the
+T=4096 non-causal prefill, the T=8192 prefill with a 4096-key sliding window
+and a packed batch of 32 sequences of 128..8192 tokens.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
-oracle on a bounded sample of the same workload instead.
+oracle on a bounded sample of the same workload instead; ``--sweep`` prints
+the prefill time against T; ``--profile-case`` runs one named workload for ncu.
 """
 from __future__ import annotations
 
@@ -33,6 +36,7 @@ PRIMARY = "llama3_8b_prefill_bf16_b1_hq32_hkv8_t8192_d128_causal"
 DECODE = "gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128"
 PAGED_DECODE = "gqa_paged_decode_bf16_b64_hq32_hkv8_tk4096_d128_p16"
 GPT2 = "gpt2s_prefill_bf16_b8_h12_t1024_d64_causal"
+VARLEN = "llama3_8b_varlen_prefill_bf16_32seq_len128to8192_hq32_hkv8_d128_causal"
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -54,6 +58,9 @@ def parse_args():
     ap.add_argument("--profile-case", default=None, metavar="WORKLOAD",
                     help="only run --warmup + --steps calls of this named workload "
                          "(no L2 flush, clocks, e2e or baselines): the command ncu captures")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the prefill over T = 64 .. 4096 (8192) and print one JSON line "
+                         "per point (the T^2 curve); not the bench line")
     return ap.parse_args()
 
 
@@ -424,6 +431,43 @@ def run_secondary(args, attn, peaks, flush):
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
     }
+    # Sliding window of 4096 keys on the primary workload's shapes.
+    w = WORKLOADS[PRIMARY]
+    q, k, v = (x.cuda() for x in make_workload(w, 0))
+    o = torch.empty_like(q)
+    W = 4096
+    fn = lambda: attn.attn_fwd_window(q, k, v, W, out=o, want_lse=False)  # noqa: E731
+    times = time_steps(fn, steps, 5, flush)
+    ms = sum(times) / steps
+    pairs = W * (W + 1) // 2 + (w.Tq - W) * W  # visible (query, key) pairs of one head
+    tf = 4.0 * pairs * w.D * w.B * w.Hq / (ms * 1e-3) / 1e12
+    out["llama3_window4096_t8192"] = {
+        "workload": f"{PRIMARY}_window{W}", "value": round(tf, 3), "unit": "TFLOP/s",
+        "ms_per_step": round(ms, 5), "flops_per_step": 4.0 * pairs * w.D * w.B * w.Hq,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
+    }
+    del q, k, v, o
+    # Packed variable-length prefill: 32 sequences of 128..8192 tokens.
+    from transformer_attention_fwd_gb300.inputs import VARLEN_WORKLOADS, make_varlen_workload
+    vw = VARLEN_WORKLOADS[VARLEN]
+    q, k, v, cq, ck = (x.cuda() for x in make_varlen_workload(vw, 0))
+    o = torch.empty_like(q)
+    lse = torch.empty((vw.Hq, q.shape[0]), dtype=torch.float32, device="cuda")
+    fn = lambda: attn.attn_fwd_varlen(q, k, v, cq, ck, vw.causal, out=o, lse=lse)  # noqa: E731
+    fn()
+    _, _, kernels = attn.last_launch_info()
+    times = time_steps(fn, steps, 5, flush)
+    ms = sum(times) / steps
+    tf = vw.flops() / (ms * 1e-3) / 1e12
+    out["llama3_varlen_mix"] = {
+        "workload": VARLEN, "value": round(tf, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+        "flops_per_step": vw.flops(), "tokens": int(q.shape[0]), "kernels_per_step": kernels,
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None,
+                     "note": "step time includes the two scheduling kernels"},
+    }
+    del q, k, v, cq, ck, o, lse
     assert attn.device_status() == attn.ATTN_OK, attn.last_error()
     return out
 
@@ -473,6 +517,18 @@ def run_profile_case(args):
     from transformer_attention_fwd_gb300 import attn
     from transformer_attention_fwd_gb300.inputs import (PAGED_WORKLOADS, WORKLOADS,
                                                         make_paged_workload, make_workload)
+    from transformer_attention_fwd_gb300.inputs import VARLEN_WORKLOADS, make_varlen_workload
+    if args.profile_case in VARLEN_WORKLOADS:
+        vw = VARLEN_WORKLOADS[args.profile_case]
+        q, k, v, cq, ck = (x.cuda() for x in make_varlen_workload(vw, 0))
+        fn = lambda: attn.attn_fwd_varlen(q, k, v, cq, ck, vw.causal)  # noqa: E731
+        times = time_steps(fn, args.steps, args.warmup)
+        if attn.device_status() != attn.ATTN_OK:
+            raise RuntimeError(attn.last_error())
+        ms = sum(times) / len(times)
+        print(json.dumps({"profile_case": vw.name, "ms_per_step": round(ms, 5),
+                          "tflops": round(vw.flops() / (ms * 1e-3) / 1e12, 3)}), flush=True)
+        return 0
     if args.profile_case in PAGED_WORKLOADS:
         pw = PAGED_WORKLOADS[args.profile_case]
         q, kv, bt, sl = (x.cuda() for x in make_paged_workload(pw, 0))
@@ -500,10 +556,53 @@ def run_profile_case(args):
     return 0
 
 
+SWEEP_SHAPES = [
+    # (name, B, Hq, Hkv, D, causal, largest T)
+    ("mha_b1_h4_d64", 1, 4, 4, 64, False, 4096),
+    ("llama3_8b_b1_hq32_hkv8_d128_causal", 1, 32, 8, 128, True, 8192),
+]
+
+
+def run_sweep(args):
+    """Prefill time against sequence length: T = 64, 128, .., doubling. The
+    growth column is t(T) / t(T/2), which tends to 4 once the T^2 work
+    dominates the launch and pipeline-fill latency."""
+    import torch
+    from transformer_attention_fwd_gb300 import build as b
+    b.build()
+    from transformer_attention_fwd_gb300 import attn
+    from transformer_attention_fwd_gb300.inputs import make_qkv
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.fill_(1)  # noqa: E731
+    steps = max(5, min(args.steps, 200))
+    for name, B, Hq, Hkv, D, causal, tmax in SWEEP_SHAPES:
+        prev = None
+        T = 64
+        while T <= tmax:
+            q, k, v = (x.cuda() for x in make_qkv(B, Hq, Hkv, T, T, D, "bf16", 0))
+            o = torch.empty_like(q)
+            fn = lambda: attn.attn_fwd(q, k, v, causal=causal, out=o, want_lse=False)  # noqa: E731
+            times = time_steps(fn, steps, max(3, args.warmup), flush)
+            ms = sum(times) / steps
+            flops = 4.0 * B * Hq * T * T * D * (0.5 if causal else 1.0)
+            print(json.dumps({"sweep": name, "T": T, "ms_per_step": round(ms, 5),
+                              "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+                              "growth": None if prev is None else round(ms / prev, 3)}),
+                  flush=True)
+            prev = ms
+            T *= 2
+            del q, k, v, o
+    if attn.device_status() != attn.ATTN_OK:
+        raise RuntimeError(attn.last_error())
+    return 0
+
+
 def main():
     args = parse_args()
     if args.profile_case:
         return run_profile_case(args)
+    if args.sweep:
+        return run_sweep(args)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

@@ -144,6 +144,57 @@ attn_status attn_fwd_decode_noalloc(const void* q, const void* k, const void* v,
                                     cudaStream_t stream);
 
 /*
+ * attn_fwd_window -- causal attention with a sliding window ("第 11 章 ·
+ * Attention 入门" §11.8.4, Sliding Window Attention: each query attends only
+ * to the most recent `window` tokens).  Query row i, at position
+ * i + (Tk - Tq) of the key sequence, sees keys i + (Tk - Tq) - window + 1 ..
+ * i + (Tk - Tq) (clamped at 0): its own position and the window - 1 before
+ * it.  Key tiles wholly outside every row's window are never visited.
+ * bf16 only (ATTN_F32 returns ATTN_ERR_UNSUPPORTED); any Tq >= 1 runs on the
+ * tensor-core prefill kernel.  window >= 1 (window >= Tk is plain causal
+ * attention).  Otherwise the arguments, layouts and errors of attn_fwd with
+ * causal = 1.
+ */
+attn_status attn_fwd_window(const void* q, const void* k, const void* v,
+                            void* o, float* lse, int B, int Hq, int Hkv,
+                            int Tq, int Tk, int D, int window, float scale,
+                            attn_dtype dtype, cudaStream_t stream);
+
+/*
+ * attn_fwd_varlen -- bf16 attention over variable-length sequences packed
+ * back to back along the token axis, in the (T, H, D) layout of "第 11 章 ·
+ * Attention 入门", 11.11.  Each sequence is its own attention problem: with
+ * causal = 1 its query rows are aligned to the end of its keys (a chunk of
+ * new tokens against a longer history, §11.8.2), and window > 0 adds the
+ * sliding window of attn_fwd_window (§11.8.4).
+ *   q, o:   [total_q, Hq, D] bf16, 16-byte aligned.
+ *   k, v:   [total_k, Hkv, D] bf16, 16-byte aligned.
+ *   cu_seqlens_q, cu_seqlens_k: [B + 1] int32, device.  Sequence b owns
+ *           query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
+ *           cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.
+ *   lse:    [Hq, total_q] float32 or NULL (natural-log log-sum-exp).
+ *   D 64 or 128; Hq a multiple of Hkv (GQA); window >= 0 (0: none; > 0 needs
+ *   causal); scale > 0.
+ * A sequence with queries but no keys gets O = 0 and lse = -inf.  Rows of o
+ * (and lse) outside every sequence are not written.  Key and value rows past
+ * a sequence's end share a tile with it and are multiplied by an exact zero
+ * weight, so every row of k and v up to total_k must hold finite values.
+ * Device-side checks: offsets outside 0 .. total, decreasing offsets, or a
+ * causal sequence with more queries than keys drop that sequence (its rows
+ * are not written) and set a flag that attn_get_device_status reports as
+ * ATTN_ERR_BAD_INPUT.  Workspace (the work-item schedule) is allocated and
+ * freed on `stream`; a failed allocation returns ATTN_ERR_NO_MEMORY.
+ * Host-side argument errors as for attn_fwd (ATTN_ERR_INVALID_ARG /
+ * ATTN_ERR_UNSUPPORTED), before anything is launched.  total_q = 0 launches
+ * nothing.
+ */
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
+                            void* o, float* lse, const int* cu_seqlens_q,
+                            const int* cu_seqlens_k, int B, int Hq, int Hkv,
+                            int total_q, int total_k, int D, int causal,
+                            int window, float scale, cudaStream_t stream);
+
+/*
  * attn_fwd_decode_paged -- decode (one query row per (b, hq)) against a paged
  * KV cache ("第 11 章 · Attention 入门", 11.11, the KV-cache / VMM passage: the
  * cache is a pool of physical blocks of `page_size` tokens, each holding the K

@@ -29,6 +29,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_prefill", "attn_fwd_decode", "attn_fwd_decode_paged",
+            "attn_fwd_window", "attn_fwd_varlen",
             "attn_get_device_status", "attn_last_error", "attn_diag_mma_tile",
             "attn_diag_wait_timeout"} <= set(names)
     for n in names:
@@ -98,6 +99,44 @@ def test_paged_decode_arguments_rejected_before_launch(lib, args, code, msg):
     lib.attn_last_error.restype = ctypes.c_char_p
     assert f(*args, None) == code
     assert msg in lib.attn_last_error().decode()
+
+
+def test_window_arguments_rejected_before_launch(lib):
+    f = lib.attn_fwd_window
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
+    f.restype = ctypes.c_int
+    lib.attn_last_error.restype = ctypes.c_char_p
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 0, 0.1, 1, None) == 1
+    assert b"window" in lib.attn_last_error()
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 16, 0.1, 0, None) == 2  # fp32
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 80, 64, 128, 16, 0.1, 1, None) == 1  # Tq > Tk
+    assert f(FAKE + 4, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 16, 0.1, 1, None) == 1
+
+
+def test_varlen_arguments_rejected_before_launch(lib):
+    f = lib.attn_fwd_varlen
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
+    f.restype = ctypes.c_int
+    lib.attn_last_error.restype = ctypes.c_char_p
+
+    def call(q=FAKE, cu=FAKE, B=2, Hq=4, Hkv=2, tq=300, tk=300, D=128, causal=1, window=0,
+             scale=0.1):
+        return f(q, FAKE, FAKE, FAKE, None, cu, FAKE, B, Hq, Hkv, tq, tk, D, causal, window,
+                 scale, None)
+
+    assert call(causal=0, window=16) == 1 and b"causal" in lib.attn_last_error()
+    assert call(window=-1) == 1
+    assert call(D=96) == 2
+    assert call(Hq=6, Hkv=4) == 1
+    assert call(tq=-1) == 1
+    assert call(scale=0.0) == 1
+    assert call(q=FAKE + 4) == 1
+    assert call(cu=None) == 1
+    assert call(B=0) == 1
+    # No query rows: nothing to launch, no device needed.
+    assert call(q=None, tq=0) == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

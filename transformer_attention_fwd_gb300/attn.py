@@ -52,6 +52,8 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         "attn_fwd_prefill": [P, P, P, P, P, I, I, I, I, I, I, I, F, P],
         "attn_fwd_decode": [P, P, P, P, P, I, I, I, I, I, F, I, P],
         "attn_fwd_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P],
+        "attn_fwd_window": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
+        "attn_fwd_varlen": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P],
         "attn_get_device_status": [P],
         "attn_diag_mma_tile": [P, P, P, P, P, I, P],
         "attn_diag_wait_timeout": [LL, P],
@@ -168,6 +170,57 @@ def attn_fwd_decode(q, k, v, scale: float | None = None, num_splits: int = 0, ou
     o, lse = _outputs(q, out, lse, want_lse)
     _check(lib.attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tk, D,
                                scale, int(num_splits), _stream_handle(stream)))
+    return o, lse
+
+
+def attn_fwd_window(q, k, v, window: int, scale: float | None = None, out=None, lse=None,
+                    want_lse: bool = True, stream=None):
+    """Causal attention with a sliding window of ``window`` keys
+    (``attn_fwd_window``); bf16 [B, Hq, Tq, D] / [B, Hkv, Tk, D] CUDA tensors."""
+    B, Hq, Hkv, Tq, Tk, D = _shapes(q, k, v)
+    if q.dtype != torch.bfloat16:
+        raise ValueError("attn_fwd_window takes bf16 tensors")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o, lse = _outputs(q, out, lse, want_lse)
+    _check(lib.attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk,
+                               D, int(window), scale, ATTN_BF16, _stream_handle(stream)))
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, window: int = 0,
+                    scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+                    stream=None):
+    """Attention over sequences packed along the token axis (``attn_fwd_varlen``).
+
+    q: [total_q, Hq, D] bf16; k, v: [total_k, Hkv, D] bf16; cu_seqlens_q,
+    cu_seqlens_k: [B + 1] int32 offsets; all CUDA tensors.  Returns
+    ``(o [total_q, Hq, D], lse [Hq, total_q] or None)``.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens_q", cu_seqlens_q),
+                    ("cu_seqlens_k", cu_seqlens_k)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or q.shape[2] != k.shape[2]:
+        raise ValueError("q must be [total_q, Hq, D] and k, v [total_k, Hkv, D]")
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise ValueError("attn_fwd_varlen takes bf16 tensors")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be int32")
+    if (cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape
+            or cu_seqlens_q.shape[0] < 2):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be [B + 1]")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.shape[0] - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    _check(lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
+                               _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, D,
+                               1 if causal else 0, int(window), scale, _stream_handle(stream)))
     return o, lse
 
 

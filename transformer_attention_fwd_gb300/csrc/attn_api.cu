@@ -146,10 +146,10 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     const void* ptr;
     long long rows, slabs;
-    int D, box_rows, rank;
+    int D, box_rows, rank, packed;
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && rows == o.rows && slabs == o.slabs && D == o.D &&
-               box_rows == o.box_rows && rank == o.rank;
+               box_rows == o.box_rows && rank == o.rank && packed == o.packed;
     }
 };
 struct MapEntry {
@@ -161,10 +161,12 @@ std::vector<MapEntry> g_maps;  // most recently used last
 constexpr size_t kMapCacheSize = 64;
 
 // Tiled map over a [slabs][rows][D] bf16 tensor; box = 64 columns x box_rows
-// rows x 1 slab, 128-byte swizzle, zero fill outside the tensor.
+// rows x 1 slab, 128-byte swizzle, zero fill outside the tensor.  packed:
+// the tensor is [rows][slabs][D] instead (dims D, slabs, rows; box 64 x 1 x
+// box_rows), which lands in shared memory in the same layout.
 attn_status make_map(const void* ptr, long long rows, long long slabs, int D, int box_rows,
-                     int rank, CUtensorMap* out) {
-    const MapKey key{ptr, rows, slabs, D, box_rows, rank};
+                     int rank, CUtensorMap* out, bool packed = false) {
+    const MapKey key{ptr, rows, slabs, D, box_rows, rank, packed ? 1 : 0};
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
         for (size_t i = g_maps.size(); i-- > 0;) {
@@ -186,6 +188,13 @@ attn_status make_map(const void* ptr, long long rows, long long slabs, int D, in
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                              static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(rows)};
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    if (packed) {
+        dims[1] = static_cast<cuuint64_t>(slabs);
+        dims[2] = static_cast<cuuint64_t>(rows);
+        strides[1] = static_cast<cuuint64_t>(D) * 2 * static_cast<cuuint64_t>(slabs);
+        box[1] = 1;
+        box[2] = static_cast<cuuint32_t>(box_rows);
+    }
     cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
     CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
@@ -348,6 +357,87 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     return run_prefill(q, k, v, o, lse, s, env);
 }
 
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int Hq, int Hkv, int Tq, int Tk, int D, int window,
+                            float scale, attn_dtype dtype, cudaStream_t stream) {
+    if (dtype == ATTN_F32)
+        return fail(ATTN_ERR_UNSUPPORTED, "the sliding window is implemented for bf16 only");
+    if (dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, 1, scale);
+    if (st != ATTN_OK) return st;
+    if (window < 1) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 1 (got %d)", window);
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    Shape s{B, Hq, Hkv, Tq, Tk, D, 1, scale};
+    s.window = window;
+    return run_prefill(q, k, v, o, lse, s, env);
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
+                            int Hkv, int total_q, int total_k, int D, int causal, int window,
+                            float scale, cudaStream_t stream) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || total_q < 0 || total_k < 0)
+        return fail(ATTN_ERR_INVALID_ARG,
+                    "B, Hq, Hkv, D must be >= 1 and total_q, total_k >= 0 (got %d, %d, %d, %d, %d, %d)",
+                    B, Hq, Hkv, D, total_q, total_k);
+    if (D != 64 && D != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim D=%d not supported (64 or 128)", D);
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    if (!std::isfinite(scale) || !(scale > 0.0f))
+        return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and positive (got %g)", (double)scale);
+    if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 0 (got %d)", window);
+    if (window > 0 && !causal)
+        return fail(ATTN_ERR_INVALID_ARG, "a sliding window needs the causal mask");
+    if (total_q > 0x7fffffff - 1024 || total_k > 0x7fffffff - 1024 || B == 0x7fffffff)
+        return fail(ATTN_ERR_INVALID_ARG, "total_q and total_k must be below 2^31 - 1024");
+    if (total_q == 0) {  // nothing to compute (empty tensors may have null pointers)
+        record_launch(0, 0, 0);
+        return ok();
+    }
+    if (!q || !o || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v)))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, cu_seqlens_q and cu_seqlens_k must be non-null");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4)))
+        return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens_q, cu_seqlens_k and lse must be 4-byte aligned");
+    const VarlenShape s{B, Hq, Hkv, total_q, total_k, D, causal ? 1 : 0, window, scale};
+    const size_t bytes = varlen_workspace_bytes(s);
+    if (bytes == 0)
+        return fail(ATTN_ERR_INVALID_ARG, "too many work items (Hq * query blocks must fit in 31 bits)");
+    LaunchEnv env;
+    attn_status st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    PrefillMaps maps;
+    const int box = prefill_box_rows();
+    if (total_k > 0) {
+        if ((st = make_map(q, total_q, Hq, D, box, 3, &maps.q, true)) != ATTN_OK) return st;
+        if ((st = make_map(k, total_k, Hkv, D, box, 3, &maps.k, true)) != ATTN_OK) return st;
+        if ((st = make_map(v, total_k, Hkv, D, box, 3, &maps.v, true)) != ATTN_OK) return st;
+    }
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
+    if (e != cudaSuccess || ws == nullptr) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, "varlen workspace of %zu bytes: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    VarlenSchedule sched{};
+    int kernels = 0, grid = 0, k2 = 0;
+    e = launch_varlen_schedule(cu_seqlens_q, cu_seqlens_k, s, ws, static_cast<uint16_t*>(o), lse,
+                               env, &sched, &kernels);
+    if (e == cudaSuccess && total_k > 0) {
+        e = launch_prefill_packed_bf16(maps, static_cast<uint16_t*>(o), lse, s, sched, env, &grid,
+                                       &k2);
+        kernels += k2;
+    }
+    cudaError_t f = cudaFreeAsync(ws, env.stream);
+    if (e == cudaSuccess && f != cudaSuccess) e = f;
+    if (e != cudaSuccess) return cuda_fail(e, "varlen prefill launch");
+    record_launch(grid, sched.item_bound, kernels);
+    return ok();
+}
+
 attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache, const int* block_table,
                                   const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv,
                                   int D, int page_size, int max_pages_per_seq, int num_blocks,
@@ -416,8 +506,8 @@ attn_status attn_get_device_status(cudaStream_t stream) {
                     (word >> 8) & 0xffu);
     if (word & kBadInputBit)
         return fail(ATTN_ERR_BAD_INPUT,
-                    "a block id or sequence length was out of range (a safe substitute was used); "
-                    "outputs undefined");
+                    "a block id, sequence length or sequence offset was out of range (a safe "
+                    "substitute was used, or the sequence was skipped); outputs undefined");
     return ok();
 }
 

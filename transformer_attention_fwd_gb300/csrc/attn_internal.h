@@ -23,6 +23,7 @@ struct Shape {
     int B, Hq, Hkv, Tq, Tk, D;
     int causal;
     float scale;
+    int window = 0;  // > 0: sliding window of that many keys (causal, prefill kernel)
 };
 
 // Each launcher returns cudaSuccess or the CUDA error of its launch; argument
@@ -39,6 +40,36 @@ cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse
                                 const Shape& s, const LaunchEnv& env, int* grid_out,
                                 int* items_out, int* kernels_launched);
 int prefill_block_rows();  // query rows per CTA work item
+
+// Packed variable-length prefill: q [total_q, Hq, D], k and v [total_k, Hkv,
+// D], sequence b at rows cu_q[b] .. cu_q[b+1]-1 of q and cu_k[b] ..
+// cu_k[b+1]-1 of k and v; o like q, lse [Hq, total_q].
+struct VarlenShape {
+    int B, Hq, Hkv, total_q, total_k, D;
+    int causal;
+    int window;  // > 0: sliding window (causal only)
+    float scale;
+};
+// One work item of the packed prefill: {q0, Tq, k0, Tk}, {query block, head, 0, 0}.
+struct VarlenSchedule {
+    const int4* items;     // 2 int4 per item, longest query blocks first
+    const int* n_items;    // device: number of items written
+    int item_bound;        // host: upper bound on the item count
+};
+// Workspace for the scheduling kernels (bytes); 0 if the item count could
+// overflow an int.
+size_t varlen_workspace_bytes(const VarlenShape& s);
+// Validates the offsets on the device (bad ones set ATTN_DEV_BAD_INPUT and
+// drop the sequence), writes O = 0 and lse = -inf for query rows whose
+// sequence has no keys, and lays out the work items in `ws`.
+cudaError_t launch_varlen_schedule(const int* cu_q, const int* cu_k, const VarlenShape& s,
+                                   void* ws, uint16_t* o, float* lse, const LaunchEnv& env,
+                                   VarlenSchedule* out, int* kernels_launched);
+// Tensor maps over the packed tensors (rows along dim 2) are built by the caller.
+cudaError_t launch_prefill_packed_bf16(const PrefillMaps& maps, uint16_t* o, float* lse,
+                                       const VarlenShape& s, const VarlenSchedule& sched,
+                                       const LaunchEnv& env, int* grid_out,
+                                       int* kernels_launched);
 int prefill_box_rows();    // rows of one TMA box (Q, K and V tiles)
 
 // Split-KV decode.  ws_o: [B*Hq, splits, D] fp32, ws_lse: [B*Hq, splits] fp32

@@ -31,6 +31,7 @@
 // the running reference directly.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -111,40 +112,109 @@ struct PrefillParams {
     uint16_t* o;
     float* lse;
     int Hq, Hkv, Tq, Tk, group, causal;
+    int window;  // > 0: each row also drops keys more than window-1 before its own
     float scale_log2;
     int n_qblocks, n_bh, n_items;
+    // Packed mode ((T, H, D) tensors, sequences back to back along T): two
+    // int4 per work item (see Record) and the device-side item count
+    // (n_items is then an upper bound); total_q rows of q and o, lse
+    // [Hq, total_q].
+    const int4* items;
+    const int* n_items_dev;
+    int total_q;
     unsigned* status;
     unsigned long long limit_ns;
 };
 
+// A work item: query block qb (two 128-row tiles) of one query head.
+// Dense mode: head bh of the [B*Hq] planes, KV plane bkv, lengths p.Tq, p.Tk.
+// Packed mode (kPacked): head bh of the sequence at query rows q0.. and key
+// rows k0.. of the packed tensors, lengths Tq, Tk; bkv is the KV head.
 struct Item {
     int bh, qb, bkv;
-    int n[2];  // key tiles visited by query tile 0 / 1 (0: tile is past Tq)
+    int n[2];   // query tile t visits key tiles lo[t] .. n[t]-1 (n = 0: tile is past Tq)
+    int lo[2];  // first key tile holding a key of the tile's first row's window
+    int q0, k0, Tq, Tk;  // packed mode only
 };
 
-// Work item idx -> (bh, query block).  Query blocks are numbered from the
-// last (longest under the causal mask) to the first.
-__device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p) {
+// One packed-mode work item, as the scheduling kernels write it:
+// {q0, Tq, k0, Tk}, {query block, head, -, -}.
+struct Record {
+    int4 r[2];
+};
+
+// Work item idx -> head and query block.  Dense: query blocks are numbered
+// from the last (longest under the causal mask) to the first.  Packed: the
+// item's record is passed in (the scheduling kernels use the same order).
+template <bool kPacked>
+__device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p, const Record& rec) {
     Item it;
-    const int qrev = idx / p.n_bh;
-    it.bh = idx - qrev * p.n_bh;
-    it.qb = p.n_qblocks - 1 - qrev;
-    const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
-    it.bkv = b * p.Hkv + hq / p.group;
+    int Tq, Tk;
+    if constexpr (!kPacked) {
+        const int qrev = idx / p.n_bh;
+        it.bh = idx - qrev * p.n_bh;
+        it.qb = p.n_qblocks - 1 - qrev;
+        const int b = it.bh / p.Hq, hq = it.bh - b * p.Hq;
+        it.bkv = b * p.Hkv + hq / p.group;
+        Tq = p.Tq;
+        Tk = p.Tk;
+    } else {
+        it.q0 = rec.r[0].x;
+        it.Tq = Tq = rec.r[0].y;
+        it.k0 = rec.r[0].z;
+        it.Tk = Tk = rec.r[0].w;
+        it.qb = rec.r[1].x;
+        it.bh = rec.r[1].y;
+        it.bkv = it.bh / p.group;
+    }
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
         const int r0 = it.qb * kItemRows + t * BM;
-        if (r0 >= p.Tq) {
+        it.lo[t] = 0;
+        if (p.window > 0 && r0 < Tq) {
+            const int first_key = r0 + (Tk - Tq) - p.window + 1;  // of row r0
+            it.lo[t] = first_key > 0 ? first_key / BN : 0;
+        }
+        if (r0 >= Tq) {
             it.n[t] = 0;
         } else if (p.causal) {
-            const int rlast = min(r0 + BM - 1, p.Tq - 1);
-            const int kmax = min(p.Tk - 1, rlast + (p.Tk - p.Tq));
+            const int rlast = min(r0 + BM - 1, Tq - 1);
+            const int kmax = min(Tk - 1, rlast + (Tk - Tq));
             it.n[t] = kmax / BN + 1;
         } else {
-            it.n[t] = (p.Tk + BN - 1) / BN;
+            it.n[t] = (Tk + BN - 1) / BN;
         }
     }
     return it;
+}
+
+// Packed mode: the record of item idx.  The next item's record is pulled
+// into L1 at the same time, so the load that starts the next item hits L1
+// instead of waiting on L2 (no registers are held across the item for it).
+template <bool kPacked>
+__device__ __forceinline__ Record fetch_record(const PrefillParams& p, int idx, int next_idx) {
+    Record rec;
+    if constexpr (kPacked) {
+        if (next_idx >= 0)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p.items + 2 * static_cast<int64_t>(next_idx)));
+        rec.r[0] = __ldg(p.items + 2 * static_cast<int64_t>(idx));
+        rec.r[1] = __ldg(p.items + 2 * static_cast<int64_t>(idx) + 1);
+    } else {
+        rec.r[0] = rec.r[1] = make_int4(0, 0, 0, 0);
+    }
+    return rec;
+}
+
+// TMA coordinates (dims 1, 2) of query row r / key row r of an item.  Dense
+// tensors are viewed as [B*H][T][D] (rows along dim 1), packed ones as
+// [T][H][D] (rows along dim 2).
+template <bool kPacked>
+__device__ __forceinline__ int2 q_coord(const Item& it, int r) {
+    return kPacked ? make_int2(it.bh, it.q0 + r) : make_int2(r, it.bh);
+}
+template <bool kPacked>
+__device__ __forceinline__ int2 k_coord(const Item& it, int r) {
+    return kPacked ? make_int2(it.bkv, it.k0 + r) : make_int2(r, it.bkv);
 }
 
 // The k-th item of this CTA: the longest-first list is dealt in passes of
@@ -233,16 +303,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // ----------------------------------------------------------------------------
 // Roles
 // ----------------------------------------------------------------------------
-template <int D>
+template <int D, bool kPacked>
 __device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint8_t* smem,
-                            Bars* bars, const PrefillParams& p, const WaitGuard& g) {
+                            Bars* bars, const PrefillParams& p, int n_items, const WaitGuard& g) {
     using C = Cfg<D>;
     uint32_t kv_it = 0, q_it = 0;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
-        const int idx = snake_item(k, p.n_items);
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int idx = snake_item(k, n_items);
         if (idx < 0) continue;
-        const Item it = decode_item(idx, p);
+        const Item it = decode_item<kPacked>(
+            idx, p, fetch_record<kPacked>(p, idx, snake_item(k + 1, n_items)));
         const int nkv = max(it.n[0], it.n[1]);
+        const int j0 = it.lo[0];  // tile 0's window starts first
         const int qs = q_it % C::kQStages;
         const uint32_t qph = (q_it / C::kQStages) & 1;
         if (q_it >= (uint32_t)C::kQStages &&
@@ -253,23 +325,24 @@ __device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
             if (it.n[t] == 0) continue;
+            const int2 xy = q_coord<kPacked>(it, it.qb * kItemRows + t * BM);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(smem + C::kQOff + (qs * NQT + t) * C::kTileBytes + c * kBoxBytes,
-                            tmQ, &bars->q_full[qs], c * kBoxCols, it.qb * kItemRows + t * BM,
-                            it.bh);
+                            tmQ, &bars->q_full[qs], c * kBoxCols, xy.x, xy.y);
         }
         ++q_it;
-        for (int j = 0; j < nkv; ++j, ++kv_it) {
+        for (int j = j0; j < nkv; ++j, ++kv_it) {
             const int s = kv_it % C::kKStages;
             const uint32_t ph = (kv_it / C::kKStages) & 1;
             if (kv_it >= C::kKStages && !mbar_wait(&bars->k_empty[s], ph ^ 1, g, SITE_K_EMPTY))
                 goto drain;
             mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+            const int2 xy = k_coord<kPacked>(it, j * BN);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * kBoxBytes, tmK,
-                            &bars->k_full[s], c * kBoxCols, j * BN, it.bkv);
+                            &bars->k_full[s], c * kBoxCols, xy.x, xy.y);
         }
     }
     return;
@@ -281,26 +354,29 @@ drain:
         wait_quiet(&bars->k_full[i % C::kKStages], (i / C::kKStages) & 1, kDrainLimitNs);
 }
 
-template <int D>
+template <int D, bool kPacked>
 __device__ void producer_v(const CUtensorMap* tmV, uint8_t* smem, Bars* bars,
-                           const PrefillParams& p, const WaitGuard& g) {
+                           const PrefillParams& p, int n_items, const WaitGuard& g) {
     using C = Cfg<D>;
     uint32_t kv_it = 0;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
-        const int idx = snake_item(k, p.n_items);
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int idx = snake_item(k, n_items);
         if (idx < 0) continue;
-        const Item it = decode_item(idx, p);
+        const Item it = decode_item<kPacked>(
+            idx, p, fetch_record<kPacked>(p, idx, snake_item(k + 1, n_items)));
         const int nkv = max(it.n[0], it.n[1]);
-        for (int j = 0; j < nkv; ++j, ++kv_it) {
+        const int j0 = it.lo[0];  // tile 0's window starts first
+        for (int j = j0; j < nkv; ++j, ++kv_it) {
             const int s = kv_it % C::kVStages;
             const uint32_t ph = (kv_it / C::kVStages) & 1;
             if (kv_it >= C::kVStages && !mbar_wait(&bars->v_empty[s], ph ^ 1, g, SITE_V_EMPTY))
                 goto drain;
             mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+            const int2 xy = k_coord<kPacked>(it, j * BN);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
                 tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * kBoxBytes, tmV,
-                            &bars->v_full[s], c * kBoxCols, j * BN, it.bkv);
+                            &bars->v_full[s], c * kBoxCols, xy.x, xy.y);
         }
     }
     return;
@@ -309,9 +385,9 @@ drain:
         wait_quiet(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, kDrainLimitNs);
 }
 
-template <int D>
+template <int D, bool kPacked>
 __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const PrefillParams& p,
-                           const WaitGuard& g) {
+                           int n_items, const WaitGuard& g) {
     using C = Cfg<D>;
     constexpr uint32_t kTile16 = C::kTileBytes >> 4;  // one tile in descriptor units
     // Descriptors of the first Q, K and V tiles; the others are kTile16 apart.
@@ -325,61 +401,63 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
     uint32_t p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
     const uint32_t leader = elect_leader();
 
-    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
-        const int idx = snake_item(k, p.n_items);
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int idx = snake_item(k, n_items);
         if (idx < 0) continue;
-        const Item it = decode_item(idx, p);
+        const Item it = decode_item<kPacked>(
+            idx, p, fetch_record<kPacked>(p, idx, snake_item(k + 1, n_items)));
         const int n0 = it.n[0], n1 = it.n[1];
+        const int lo0 = it.lo[0], lo1 = it.lo[1];  // query tile t is active for lo_t <= j < n_t
         const int nkv = max(n0, n1);
         const uint32_t qs = q_it % C::kQStages;
         if (!warp_wait(&bars->q_full[qs], (q_it / C::kQStages) & 1, g, SITE_Q_FULL)) goto drain;
         ++q_it;
         tc_fence_after_sync();
         const uint64_t q_desc = desc_advance(q_desc0, qs * NQT * kTile16);
-        for (int j = 0; j <= nkv; ++j) {
+        for (int j = lo0; j <= nkv; ++j) {
             const uint64_t k_desc = desc_advance(k_desc0, ks * kTile16);
             const uint64_t v_desc = desc_advance(v_desc0, vs * kTile16);
             if (j < nkv) {
                 if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
-                if (j < n0) {
+                if (j >= lo0 && j < n0) {
                     issue_qk<D>(tmem + C::col_s(0), q_desc, k_desc, leader);
                     mma_commit(&bars->s_full[0], leader);
                 }
             }
-            if (j >= 1 && j - 1 < n1) {  // PV1(j-1)
+            if (j - 1 >= lo1 && j - 1 < n1) {  // PV1(j-1)
                 if (!warp_wait(&bars->p_full[1], p_cnt[1] & 1, g, SITE_P_FULL)) goto drain;
                 ++p_cnt[1];
                 if (!warp_wait(&bars->v_full[pvs], pvph, g, SITE_V_FULL)) goto drain;
-                if (j - 1 == 0 && o_cnt[1] > 0 &&
+                if (j - 1 == lo1 && o_cnt[1] > 0 &&
                     !warp_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
                     goto drain;
                 tc_fence_after_sync();
                 issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
-                            desc_advance(v_desc0, pvs * kTile16), j - 1 > 0, leader);
+                            desc_advance(v_desc0, pvs * kTile16), j - 1 > lo1, leader);
                 if (j - 1 == n1 - 1) {
                     mma_commit(&bars->o_full[1], leader);
                     ++o_cnt[1];
                 }
             }
-            if (j >= 1) mma_commit(&bars->v_empty[pvs], leader);
+            if (j > lo0) mma_commit(&bars->v_empty[pvs], leader);
             if (j < nkv) {
-                if (j < n1) {
+                if (j >= lo1 && j < n1) {
                     issue_qk<D>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc,
                                 leader);
                     mma_commit(&bars->s_full[1], leader);
                 }
                 mma_commit(&bars->k_empty[ks], leader);
                 if (j == nkv - 1) mma_commit(&bars->q_empty[qs], leader);
-                if (j < n0) {  // PV0(j)
+                if (j >= lo0 && j < n0) {  // PV0(j)
                     if (!warp_wait(&bars->p_full[0], p_cnt[0] & 1, g, SITE_P_FULL)) goto drain;
                     ++p_cnt[0];
                     if (!warp_wait(&bars->v_full[vs], vph, g, SITE_V_FULL)) goto drain;
-                    if (j == 0 && o_cnt[0] > 0 &&
+                    if (j == lo0 && o_cnt[0] > 0 &&
                         !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
-                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > 0, leader);
+                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > lo0, leader);
                     if (j == n0 - 1) {
                         mma_commit(&bars->o_full[0], leader);
                         ++o_cnt[0];
@@ -451,14 +529,18 @@ __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_l
 }
 
 // On a tile that straddles the diagonal or the end of the keys, keys past a
-// row's last visible key become -inf.
-__device__ __forceinline__ void mask_tile(uint32_t (&s)[64], int key0, int lim_a, int lim_b) {
+// row's last visible key become -inf; with a sliding window, so do keys before
+// the row's first visible key ("Attention 入门" §11.8.4, only the most recent
+// W tokens).
+__device__ __forceinline__ void mask_tile(uint32_t (&s)[64], int key0, int lim_a, int lim_b,
+                                          int lft_a, int lft_b) {
 #pragma unroll
     for (int n = 0; n < 16; ++n)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int key = key0 + 8 * n + (k & 1);
-            if (key > ((k < 2) ? lim_a : lim_b)) s[4 * n + k] = __float_as_uint(-INFINITY);
+            if (key > ((k < 2) ? lim_a : lim_b) || key < ((k < 2) ? lft_a : lft_b))
+                s[4 * n + k] = __float_as_uint(-INFINITY);
         }
 }
 
@@ -474,11 +556,11 @@ struct RowState {
 template <int D>
 __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint32_t o_addr,
                                              bool masked, int key0, int lim_a, int lim_b,
-                                             bool first, float scale_log2) {
+                                             int lft_a, int lft_b, bool first, float scale_log2) {
     uint32_t s[64];
     tmem_ld_16x256b_x16(s_addr, s);
     tmem_wait_ld64(s);
-    if (masked) mask_tile(s, key0, lim_a, lim_b);
+    if (masked) mask_tile(s, key0, lim_a, lim_b, lft_a, lft_b);
     // Fast path: weights against the running reference without a row
     // maximum.  bf16 P and the fp32 sums and accumulators have fp32's
     // exponent range, so weights far above 1 lose no relative precision; a
@@ -556,8 +638,8 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
 // warp (lane quarter warp % 4, half (warp - 4) / 4), so every tile is worked
 // on by two warps per SM sub-partition.  Per key tile the tiles are taken in
 // the order the MMA warp produces them (S0 before S1).
-template <int D>
-__device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
+template <int D, bool kPacked>
+__device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p, int n_items,
                               const WaitGuard& g) {
     using C = Cfg<D>;
     const int warp = threadIdx.x / 32;
@@ -566,38 +648,49 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
     const int ra = l0 + lane / 4;                              // rows a, a + 8 of a tile
     const int kq = 2 * (lane & 3);                             // key offset inside a chunk
     const uint32_t lanes = tmem + (static_cast<uint32_t>(l0) << 16);
-    const int off = p.Tk - p.Tq;
     uint32_t s_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
 
-    for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
-        const int idx = snake_item(k, p.n_items);
+    for (int k = 0; k * static_cast<int>(gridDim.x) < n_items; ++k) {
+        const int idx = snake_item(k, n_items);
         if (idx < 0) continue;
-        const Item it = decode_item(idx, p);
+        const Item it = decode_item<kPacked>(
+            idx, p, fetch_record<kPacked>(p, idx, snake_item(k + 1, n_items)));
         const int nkv = max(it.n[0], it.n[1]);
+        const int j0 = it.lo[0];  // tile 0's window starts first
+        const int Tq = kPacked ? it.Tq : p.Tq, Tk = kPacked ? it.Tk : p.Tk;
         RowState st[2];
-        int lim_a[2], lim_b[2], lim_first[2];
+        int lim_a[2], lim_b[2], lim_first[2], lft_a[2], lft_b[2], lft_last[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const int r0 = it.qb * kItemRows + t * BM;
             // Last visible key of rows a, b and of the tile's first row.
-            lim_a[t] = p.causal ? min(r0 + ra + off, p.Tk - 1) : p.Tk - 1;
-            lim_b[t] = p.causal ? min(r0 + ra + 8 + off, p.Tk - 1) : p.Tk - 1;
-            lim_first[t] = p.causal ? min(r0 + off, p.Tk - 1) : p.Tk - 1;
+            const int off = Tk - Tq;
+            lim_a[t] = p.causal ? min(r0 + ra + off, Tk - 1) : Tk - 1;
+            lim_b[t] = p.causal ? min(r0 + ra + 8 + off, Tk - 1) : Tk - 1;
+            lim_first[t] = p.causal ? min(r0 + off, Tk - 1) : Tk - 1;
+            // First visible key of rows a, b and of the tile's last row (window;
+            // INT_MIN without one).  The sums stay below Tk: no overflow.
+            const bool win = p.window > 0;
+            const int wl = off - p.window + 1;
+            lft_a[t] = win ? r0 + ra + wl : INT_MIN;
+            lft_b[t] = win ? r0 + ra + 8 + wl : INT_MIN;
+            lft_last[t] = win ? r0 + BM - 1 + wl : INT_MIN;
             st[t].m[0] = st[t].m[1] = -INFINITY;
             st[t].l[0] = st[t].l[1] = st[t].lr[0] = st[t].lr[1] = 0.0f;
         }
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = j0; j < nkv; ++j) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (j >= it.n[t]) continue;
+                if (j < it.lo[t] || j >= it.n[t]) continue;
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], s_cnt[t] & 1, g, SITE_S_FULL)))
                     return;
                 ++s_cnt[t];
                 tc_fence_after_sync();
                 const int kbase = j * BN;
                 softmax_tile<D>(st[t], lanes + C::col_s(t), lanes + C::col_o(t),
-                                kbase + BN - 1 > lim_first[t], kbase + kq, lim_a[t], lim_b[t],
-                                j == 0, p.scale_log2);
+                                kbase + BN - 1 > lim_first[t] || kbase < lft_last[t], kbase + kq,
+                                lim_a[t], lim_b[t], lft_a[t], lft_b[t], j == it.lo[t],
+                                p.scale_log2);
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(&bars->p_full[t]);
@@ -630,20 +723,24 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                 tmem_wait_ld(ov);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    if (row[r] >= p.Tq) continue;
-                    uint32_t* orow = reinterpret_cast<uint32_t*>(
-                        p.o + (static_cast<int64_t>(it.bh) * p.Tq + row[r]) * D + 64 * c + kq);
+                    if (row[r] >= Tq) continue;
+                    const int64_t orow =
+                        kPacked ? static_cast<int64_t>(it.q0 + row[r]) * p.Hq + it.bh
+                                : static_cast<int64_t>(it.bh) * p.Tq + row[r];
+                    uint32_t* optr =
+                        reinterpret_cast<uint32_t*>(p.o + orow * D + 64 * c + kq);
 #pragma unroll
                     for (int n = 0; n < 8; ++n)
-                        orow[4 * n] = pack_bf16x2(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
+                        optr[4 * n] = pack_bf16x2(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
                                                   __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
                 }
             }
             if ((lane & 3) == 0 && p.lse != nullptr) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
-                    if (row[r] < p.Tq)
-                        p.lse[static_cast<int64_t>(it.bh) * p.Tq + row[r]] =
+                    if (row[r] < Tq)
+                        p.lse[kPacked ? static_cast<int64_t>(it.bh) * p.total_q + it.q0 + row[r]
+                                      : static_cast<int64_t>(it.bh) * p.Tq + row[r]] =
                             (st[t].m[r] + __log2f(l[r])) * kLn2;
             }
             tc_fence_before_sync();
@@ -652,7 +749,7 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
     }
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -698,19 +795,22 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
     tc_fence_after_sync();
     const uint32_t tmem = bars->tmem_base;
     const WaitGuard g{p.status, &bars->abort, p.limit_ns};
+    // Packed sequences: the scheduling kernels counted the items; the host's
+    // figure is an upper bound.
+    const int n_items = kPacked ? min(__ldg(p.n_items_dev), p.n_items) : p.n_items;
 
     if (warp < 4) {
         regs_decrease<kCtrlRegs>();
         if (warp == 0) {
-            if (lane == 0) producer_qk<D>(&tmQ, &tmK, smem, bars, p, g);
+            if (lane == 0) producer_qk<D, kPacked>(&tmQ, &tmK, smem, bars, p, n_items, g);
         } else if (warp == 3) {
-            if (lane == 0) producer_v<D>(&tmV, smem, bars, p, g);
+            if (lane == 0) producer_v<D, kPacked>(&tmV, smem, bars, p, n_items, g);
         } else if (warp == 1) {
-            mma_issuer<D>(smem, bars, tmem, p, g);
+            mma_issuer<D, kPacked>(smem, bars, tmem, p, n_items, g);
         }
     } else {
         regs_increase<kSoftmaxRegs>();
-        softmax_group<D>(bars, tmem, p, g);
+        softmax_group<D, kPacked>(bars, tmem, p, n_items, g);
     }
 
     tc_fence_before_sync();
@@ -853,7 +953,7 @@ __global__ void diag_wait_timeout_kernel(unsigned* status, unsigned long long li
     __syncthreads();
 }
 
-template <int D>
+template <int D, bool kPacked>
 cudaError_t launch_prefill_d(const PrefillMaps& maps, const PrefillParams& prm, int grid,
                              cudaStream_t stream) {
     using C = Cfg<D>;
@@ -862,13 +962,14 @@ cudaError_t launch_prefill_d(const PrefillMaps& maps, const PrefillParams& prm, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_bf16_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_bf16_kernel<D, kPacked>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    prefill_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(maps.q, maps.k, maps.v, prm);
+    prefill_bf16_kernel<D, kPacked>
+        <<<grid, kThreads, C::kSmemBytes, stream>>>(maps.q, maps.k, maps.v, prm);
     return cudaGetLastError();
 }
 
@@ -889,20 +990,58 @@ cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse
     prm.Tk = s.Tk;
     prm.group = s.Hq / s.Hkv;
     prm.causal = s.causal;
+    prm.window = s.causal ? s.window : 0;
     prm.scale_log2 = s.scale * 1.4426950408889634f;
     prm.n_qblocks = (s.Tq + kItemRows - 1) / kItemRows;
     prm.n_bh = s.B * s.Hq;
     const long long items = static_cast<long long>(prm.n_qblocks) * prm.n_bh;
     if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prm.n_items = static_cast<int>(items);
+    prm.items = nullptr;
+    prm.n_items_dev = nullptr;
+    prm.total_q = 0;
     prm.status = env.status;
     prm.limit_ns = env.wait_limit_ns;
     const int grid = static_cast<int>(items < env.num_sms ? items : env.num_sms);
     if (grid_out) *grid_out = grid;
     if (items_out) *items_out = prm.n_items;
     if (kernels_launched) *kernels_launched = 1;
-    return (s.D == 64) ? launch_prefill_d<64>(maps, prm, grid, env.stream)
-                       : launch_prefill_d<128>(maps, prm, grid, env.stream);
+    return (s.D == 64) ? launch_prefill_d<64, false>(maps, prm, grid, env.stream)
+                       : launch_prefill_d<128, false>(maps, prm, grid, env.stream);
+}
+
+cudaError_t launch_prefill_packed_bf16(const PrefillMaps& maps, uint16_t* o, float* lse,
+                                       const VarlenShape& s, const VarlenSchedule& sched,
+                                       const LaunchEnv& env, int* grid_out,
+                                       int* kernels_launched) {
+    PrefillParams prm;
+    prm.o = o;
+    prm.lse = lse;
+    prm.Hq = s.Hq;
+    prm.Hkv = s.Hkv;
+    prm.Tq = 0;
+    prm.Tk = 0;
+    prm.group = s.Hq / s.Hkv;
+    prm.causal = s.causal;
+    prm.window = s.causal ? s.window : 0;
+    prm.scale_log2 = s.scale * 1.4426950408889634f;
+    prm.n_qblocks = 0;
+    prm.n_bh = 0;
+    prm.n_items = sched.item_bound;
+    prm.items = sched.items;
+    prm.n_items_dev = sched.n_items;
+    prm.total_q = s.total_q;
+    prm.status = env.status;
+    prm.limit_ns = env.wait_limit_ns;
+    const int grid = sched.item_bound < env.num_sms ? sched.item_bound : env.num_sms;
+    if (grid_out) *grid_out = grid;
+    if (grid < 1) {
+        if (kernels_launched) *kernels_launched = 0;
+        return cudaSuccess;
+    }
+    if (kernels_launched) *kernels_launched = 1;
+    return (s.D == 64) ? launch_prefill_d<64, true>(maps, prm, grid, env.stream)
+                       : launch_prefill_d<128, true>(maps, prm, grid, env.stream);
 }
 
 cudaError_t launch_diag_mma_tile(const CUtensorMap& a, const CUtensorMap& b,

@@ -158,3 +158,64 @@ def make_paged(B: int, Hq: int, Hkv: int, D: int, page: int, seq_lens, seed: int
 
 def make_paged_workload(w: PagedWorkload, seed: int = 0):
     return make_paged(w.B, w.Hq, w.Hkv, w.D, w.page, [w.seq_len] * w.B, seed)
+
+
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """Prefill of `n_seq` sequences of mixed length packed along the token
+    axis ((T, H, D) tensors, "第 11 章 · Attention 入门", 11.11).  Lengths are
+    drawn log-uniformly in [min_len, max_len] from a seeded generator, so short
+    and long sequences share one launch; each sequence attends only to itself
+    (Tq = Tk per sequence)."""
+    name: str
+    n_seq: int
+    min_len: int
+    max_len: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool
+    len_seed: int = 0
+
+    def seqlens(self) -> list[int]:
+        g = torch.Generator().manual_seed(int(self.len_seed))
+        u = torch.rand(self.n_seq, generator=g, dtype=torch.float64)
+        lo, hi = torch.log(torch.tensor(float(self.min_len))), torch.log(torch.tensor(float(self.max_len)))
+        return [int(x) for x in torch.exp(lo + u * (hi - lo)).round().to(torch.int64)]
+
+    def flops(self) -> float:
+        """Score and P.V multiply-adds, 4 flops per visible (query, key) pair
+        and head dimension, with the causal pair count taken as T^2 / 2."""
+        pairs = sum(L * L * (0.5 if self.causal else 1.0) for L in self.seqlens())
+        return 4.0 * pairs * self.D * self.Hq
+
+
+VARLEN_WORKLOADS = {
+    "llama3_8b_varlen_prefill_bf16_32seq_len128to8192_hq32_hkv8_d128_causal":
+        VarlenWorkload("llama3_8b_varlen_prefill_bf16_32seq_len128to8192_hq32_hkv8_d128_causal",
+                       32, 128, 8192, 32, 8, 128, True),
+}
+
+
+def make_varlen(seqlens_q, seqlens_k, Hq: int, Hkv: int, D: int, seed: int = 0):
+    """Draw a packed variable-length problem on the CPU: q [sum Tq, Hq, D],
+    k and v [sum Tk, Hkv, D], iid N(0, 1) rounded to bf16, and the int32
+    offsets cu_seqlens_q, cu_seqlens_k [B + 1] (sequence b at rows cu[b] ..
+    cu[b+1]-1)."""
+    g = torch.Generator().manual_seed(int(seed))
+    lq = [int(x) for x in seqlens_q]
+    lk = [int(x) for x in seqlens_k]
+    if len(lq) != len(lk):
+        raise ValueError("seqlens_q and seqlens_k differ in length")
+    tq, tk = sum(lq), sum(lk)
+    q = torch.randn(tq, Hq, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    cq = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
+    ck = torch.tensor([0] + lk, dtype=torch.int64).cumsum(0).to(torch.int32)
+    return q, k, v, cq, ck
+
+
+def make_varlen_workload(w: VarlenWorkload, seed: int = 0):
+    L = w.seqlens()
+    return make_varlen(L, L, w.Hq, w.Hkv, w.D, seed)
