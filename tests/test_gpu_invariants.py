@@ -155,3 +155,23 @@ def test_rising_scores_take_the_exact_path(causal, Tq):
     check_status(a)
     o_ref, lse_ref = oracle.attention_f64(q, k, v, causal)
     compare(o, lse, o_ref, lse_ref, TOL_O_BF16, 1e-3 * max(1.0, float(abs(lse_ref).max())) / 10)
+
+
+@pytest.mark.parametrize("offset", [-30.0, -12.0, 12.0, 30.0])
+@pytest.mark.parametrize("causal", [True, False])
+def test_first_tile_far_from_the_reference(offset, causal):
+    """Every score of a row far above 2^62 or far below 2^-60 (in base 2):
+    weights taken against any fixed reference such as 0 would overflow or
+    vanish, so the reference must come from the row's own scores.  The
+    output must still match the oracle."""
+    a = attn()
+    g = torch.Generator().manual_seed(70)
+    T, D = 384, 64
+    q = (torch.ones(1, 2, T, D) + 0.1 * torch.randn(1, 2, T, D, generator=g)).to(torch.bfloat16)
+    k = (offset + 0.5 * torch.randn(1, 2, T, D, generator=g)).to(torch.bfloat16)
+    v = torch.randn(1, 2, T, D, generator=g).to(torch.bfloat16)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=causal)
+    check_status(a)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, causal)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, 1e-3 * max(1.0, float(abs(lse_ref).max())) / 10)

@@ -668,13 +668,14 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
             lim_a[t] = p.causal ? min(r0 + ra + off, Tk - 1) : Tk - 1;
             lim_b[t] = p.causal ? min(r0 + ra + 8 + off, Tk - 1) : Tk - 1;
             lim_first[t] = p.causal ? min(r0 + off, Tk - 1) : Tk - 1;
-            // First visible key of rows a, b and of the tile's last row (window;
-            // INT_MIN without one).  The sums stay below Tk: no overflow.
+            // First visible key of rows a, b and of the tile's last row inside
+            // Tq (window; INT_MIN without one).  The sums stay below Tk + BM:
+            // no overflow.
             const bool win = p.window > 0;
             const int wl = off - p.window + 1;
             lft_a[t] = win ? r0 + ra + wl : INT_MIN;
             lft_b[t] = win ? r0 + ra + 8 + wl : INT_MIN;
-            lft_last[t] = win ? r0 + BM - 1 + wl : INT_MIN;
+            lft_last[t] = win ? min(r0 + BM - 1, Tq - 1) + wl : INT_MIN;
             st[t].m[0] = st[t].m[1] = -INFINITY;
             st[t].l[0] = st[t].l[1] = st[t].lr[0] = st[t].lr[1] = 0.0f;
         }
