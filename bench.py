@@ -7,7 +7,7 @@ inputs already resident in HBM.  The same run also times, under "secondary":
 the stream-K decode (B=64, Hq=32, Hkv=8, Tk=4096, D=128) on a dense and on a
 paged cache, the GPT-2-small-shaped prefill (B=8, H=12, T=1024, D=64), the
 T=4096 non-causal prefill, the T=8192 prefill with a 4096-key sliding window
-and a packed batch of 32 sequences of 128..8192 tokens.
+and with fp16 I/O, and a packed batch of 32 sequences of 128..8192 tokens.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
 oracle on a bounded sample of the same workload instead; ``--sweep`` prints
@@ -356,7 +356,7 @@ def run_ours(args, rank, world):
 
 def run_secondary(args, attn, peaks, flush):
     import torch
-    from transformer_attention_fwd_gb300.inputs import WORKLOADS, make_workload
+    from transformer_attention_fwd_gb300.inputs import WORKLOADS, make_qkv, make_workload
     out = {}
     steps = max(5, min(args.steps, 100))
     # Decode: K+V = 1 GiB >> L2, no flush needed.
@@ -446,6 +446,21 @@ def run_secondary(args, attn, peaks, flush):
         "ms_per_step": round(ms, 5), "flops_per_step": 4.0 * pairs * w.D * w.B * w.Hq,
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
+    }
+    del q, k, v, o
+    # The primary workload with fp16 I/O.
+    q, k, v = (x.cuda() for x in make_qkv(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.D, "f16", 0))
+    o = torch.empty_like(q)
+    fn = lambda: attn.attn_fwd(q, k, v, causal=True, out=o, want_lse=False)  # noqa: E731
+    times = time_steps(fn, steps, 5, flush)
+    ms = sum(times) / steps
+    tf = w.flops / (ms * 1e-3) / 1e12
+    out["llama3_f16_t8192"] = {
+        "workload": PRIMARY.replace("bf16", "f16"), "value": round(tf, 3), "unit": "TFLOP/s",
+        "ms_per_step": round(ms, 5),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None,
+                     "note": "fp16 and bf16 share the measured dense peak"},
     }
     del q, k, v, o
     # Packed variable-length prefill: 32 sequences of 128..8192 tokens.

@@ -57,7 +57,7 @@ typedef enum {
     ATTN_ERR_BAD_INPUT = 6    /* a kernel found a device-side index out of range */
 } attn_status;
 
-typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_F16 = 2 } attn_dtype;
 
 /*
  * attn_fwd -- attention forward, dispatching on dtype and Tq.
@@ -65,6 +65,10 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *                         count; "Attention 入门" §11.8.2: decode streams
  *                         K/V from the cache with a 1 x N query).
  *   ATTN_BF16, Tq >= 2 -> tensor-core prefill (attn_fwd_prefill).
+ *   ATTN_F16           -> the same two paths with fp16 q, k, v and o (the
+ *                         16-bit I/O of "Attention 入门" §11.8.5, fp32
+ *                         accumulation): P is rounded to fp16 for the P.V
+ *                         product, and the decode is the automatic mode.
  *   ATTN_F32           -> float32 tiled kernel on the CUDA cores.
  * scale multiplies the raw dot products; callers normally pass 1/sqrt(D)
  * ("Attention 入门" §11.1; "Self-Attention机制深入理解" §3.3, §6).
@@ -150,8 +154,8 @@ attn_status attn_fwd_decode_noalloc(const void* q, const void* k, const void* v,
  * i + (Tk - Tq) of the key sequence, sees keys i + (Tk - Tq) - window + 1 ..
  * i + (Tk - Tq) (clamped at 0): its own position and the window - 1 before
  * it.  Key tiles wholly outside every row's window are never visited.
- * bf16 only (ATTN_F32 returns ATTN_ERR_UNSUPPORTED); any Tq >= 1 runs on the
- * tensor-core prefill kernel.  window >= 1 (window >= Tk is plain causal
+ * bf16 or fp16 (ATTN_F32 returns ATTN_ERR_UNSUPPORTED); any Tq >= 1 runs on
+ * the tensor-core prefill kernel.  window >= 1 (window >= Tk is plain causal
  * attention).  Otherwise the arguments, layouts and errors of attn_fwd with
  * causal = 1.
  */

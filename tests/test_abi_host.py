@@ -60,6 +60,8 @@ FAKE = 0x10000  # aligned, never dereferenced: validation fails first
     ((FAKE, FAKE, FAKE, FAKE, None, 0, 1, 1, 4, 4, 64, 0, 0.125, 1), 1, ">= 1"),
     ((FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1, 0, 4, 64, 0, 0.125, 1), 1, ">= 1"),
     ((FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1, 4, 4, 64, 0, 0.125, 7), 1, "dtype"),
+    ((FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1, 4, 4, 96, 1, 0.125, 2), 2, "D=96"),   # fp16
+    ((FAKE, FAKE, FAKE, FAKE, None, 1, 1, 1, 8, 4, 64, 1, 0.125, 2), 1, "Tq <= Tk"),  # fp16
 ])
 def test_invalid_arguments_rejected_before_launch(lib, args, code, msg):
     f = _fwd(lib)
@@ -112,6 +114,8 @@ def test_window_arguments_rejected_before_launch(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 16, 0.1, 0, None) == 2  # fp32
     assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 80, 64, 128, 16, 0.1, 1, None) == 1  # Tq > Tk
     assert f(FAKE + 4, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 16, 0.1, 1, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 16, 0.1, 3, None) == 1  # dtype
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 0, 0.1, 2, None) == 1  # fp16, W=0
 
 
 def test_varlen_arguments_rejected_before_launch(lib):

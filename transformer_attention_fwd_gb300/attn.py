@@ -26,6 +26,7 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_BAD_INPUT = 6
 ATTN_F32 = 0
 ATTN_BF16 = 1
+ATTN_F16 = 2
 
 STATUS_NAMES = {
     ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
@@ -126,7 +127,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
              want_lse: bool = True, stream=None):
     """O = softmax(Q K^T * scale + causal mask) V through ``attn_fwd``.
 
-    q: [B, Hq, Tq, D], k/v: [B, Hkv, Tk, D], all fp32 or all bf16 CUDA tensors.
+    q: [B, Hq, Tq, D], k/v: [B, Hkv, Tk, D], all fp32, all bf16 or all fp16 CUDA
+    tensors.
     Returns ``(o, lse)``; ``lse`` (fp32 [B, Hq, Tq]) is None if not wanted.
     ``scale`` defaults to 1/sqrt(D).
     """
@@ -135,6 +137,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
         dt = ATTN_F32
     elif q.dtype == torch.bfloat16:
         dt = ATTN_BF16
+    elif q.dtype == torch.float16:
+        dt = ATTN_F16
     else:
         raise ValueError(f"unsupported dtype {q.dtype}")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
@@ -178,12 +182,14 @@ def attn_fwd_window(q, k, v, window: int, scale: float | None = None, out=None, 
     """Causal attention with a sliding window of ``window`` keys
     (``attn_fwd_window``); bf16 [B, Hq, Tq, D] / [B, Hkv, Tk, D] CUDA tensors."""
     B, Hq, Hkv, Tq, Tk, D = _shapes(q, k, v)
-    if q.dtype != torch.bfloat16:
-        raise ValueError("attn_fwd_window takes bf16 tensors")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("attn_fwd_window takes bf16 or fp16 tensors")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     o, lse = _outputs(q, out, lse, want_lse)
     _check(lib.attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk,
-                               D, int(window), scale, ATTN_BF16, _stream_handle(stream)))
+                               D, int(window), scale,
+                               ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16,
+                               _stream_handle(stream)))
     return o, lse
 
 

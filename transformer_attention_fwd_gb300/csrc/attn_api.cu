@@ -146,10 +146,10 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     const void* ptr;
     long long rows, slabs;
-    int D, box_rows, rank, packed;
+    int D, box_rows, rank, packed, f16;
     bool operator==(const MapKey& o) const {
         return ptr == o.ptr && rows == o.rows && slabs == o.slabs && D == o.D &&
-               box_rows == o.box_rows && rank == o.rank && packed == o.packed;
+               box_rows == o.box_rows && rank == o.rank && packed == o.packed && f16 == o.f16;
     }
 };
 struct MapEntry {
@@ -160,13 +160,14 @@ std::mutex g_map_mutex;
 std::vector<MapEntry> g_maps;  // most recently used last
 constexpr size_t kMapCacheSize = 64;
 
-// Tiled map over a [slabs][rows][D] bf16 tensor; box = 64 columns x box_rows
-// rows x 1 slab, 128-byte swizzle, zero fill outside the tensor.  packed:
-// the tensor is [rows][slabs][D] instead (dims D, slabs, rows; box 64 x 1 x
-// box_rows), which lands in shared memory in the same layout.
+// Tiled map over a [slabs][rows][D] bf16 (f16: fp16) tensor; box = 64
+// columns x box_rows rows x 1 slab, 128-byte swizzle, zero fill outside the
+// tensor.  packed: the tensor is [rows][slabs][D] instead (dims D, slabs,
+// rows; box 64 x 1 x box_rows), which lands in shared memory in the same
+// layout.
 attn_status make_map(const void* ptr, long long rows, long long slabs, int D, int box_rows,
-                     int rank, CUtensorMap* out, bool packed = false) {
-    const MapKey key{ptr, rows, slabs, D, box_rows, rank, packed ? 1 : 0};
+                     int rank, CUtensorMap* out, bool packed = false, bool f16 = false) {
+    const MapKey key{ptr, rows, slabs, D, box_rows, rank, packed ? 1 : 0, f16 ? 1 : 0};
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
         for (size_t i = g_maps.size(); i-- > 0;) {
@@ -197,7 +198,8 @@ attn_status make_map(const void* ptr, long long rows, long long slabs, int D, in
     }
     cuuint32_t estr[3] = {1, 1, 1};
     CUtensorMap m;
-    CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+    CUresult r = fn(&m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    static_cast<cuuint32_t>(rank),
                     const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -222,11 +224,13 @@ attn_status run_prefill(const void* q, const void* k, const void* v, void* o, fl
                         const Shape& s, const LaunchEnv& env) {
     PrefillMaps maps;
     const int box = prefill_box_rows();
-    attn_status st = make_map(q, s.Tq, static_cast<long long>(s.B) * s.Hq, s.D, box, 3, &maps.q);
+    const bool f16 = s.f16 != 0;
+    attn_status st = make_map(q, s.Tq, static_cast<long long>(s.B) * s.Hq, s.D, box, 3, &maps.q,
+                              false, f16);
     if (st != ATTN_OK) return st;
-    st = make_map(k, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.k);
+    st = make_map(k, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.k, false, f16);
     if (st != ATTN_OK) return st;
-    st = make_map(v, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.v);
+    st = make_map(v, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.v, false, f16);
     if (st != ATTN_OK) return st;
     int grid = 0, items = 0, kernels = 0;
     cudaError_t e = launch_prefill_bf16(maps, static_cast<uint16_t*>(o), lse, s, env, &grid,
@@ -334,14 +338,15 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v, void* o
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int Hq, int Hkv, int Tq, int Tk, int D, int causal, float scale,
                      attn_dtype dtype, cudaStream_t stream) {
-    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16)
         return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
     attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, causal, scale);
     if (st != ATTN_OK) return st;
     LaunchEnv env;
     st = device_env(stream, &env);
     if (st != ATTN_OK) return st;
-    const Shape s{B, Hq, Hkv, Tq, Tk, D, causal ? 1 : 0, scale};
+    Shape s{B, Hq, Hkv, Tq, Tk, D, causal ? 1 : 0, scale};
+    s.f16 = dtype == ATTN_F16 ? 1 : 0;
     if (dtype == ATTN_F32) {
         int kernels = 0;
         cudaError_t e = launch_simt_f32(static_cast<const float*>(q), static_cast<const float*>(k),
@@ -361,8 +366,9 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
                             int B, int Hq, int Hkv, int Tq, int Tk, int D, int window,
                             float scale, attn_dtype dtype, cudaStream_t stream) {
     if (dtype == ATTN_F32)
-        return fail(ATTN_ERR_UNSUPPORTED, "the sliding window is implemented for bf16 only");
-    if (dtype != ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+        return fail(ATTN_ERR_UNSUPPORTED, "the sliding window is implemented for 16-bit I/O only");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
     attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, 1, scale);
     if (st != ATTN_OK) return st;
     if (window < 1) return fail(ATTN_ERR_INVALID_ARG, "window must be >= 1 (got %d)", window);
@@ -371,6 +377,7 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
     if (st != ATTN_OK) return st;
     Shape s{B, Hq, Hkv, Tq, Tk, D, 1, scale};
     s.window = window;
+    s.f16 = dtype == ATTN_F16 ? 1 : 0;
     return run_prefill(q, k, v, o, lse, s, env);
 }
 

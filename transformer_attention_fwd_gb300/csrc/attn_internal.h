@@ -24,6 +24,7 @@ struct Shape {
     int causal;
     float scale;
     int window = 0;  // > 0: sliding window of that many keys (causal, prefill kernel)
+    int f16 = 0;     // 16-bit I/O is fp16 instead of bf16 (prefill and stream-K decode)
 };
 
 // Each launcher returns cudaSuccess or the CUDA error of its launch; argument

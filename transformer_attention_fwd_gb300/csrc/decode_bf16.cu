@@ -46,11 +46,14 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint16_t* p) {
     return r;
 }
 
+// Eight 16-bit elements (bf16, or fp16 with kF16) -> fp32 (exact).
+template <bool kF16 = false>
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-    f[0] = bf16_lo_to_f32(u.x); f[1] = bf16_hi_to_f32(u.x);
-    f[2] = bf16_lo_to_f32(u.y); f[3] = bf16_hi_to_f32(u.y);
-    f[4] = bf16_lo_to_f32(u.z); f[5] = bf16_hi_to_f32(u.z);
-    f[6] = bf16_lo_to_f32(u.w); f[7] = bf16_hi_to_f32(u.w);
+    using E = Elem16<kF16>;
+    f[0] = E::lo(u.x); f[1] = E::hi(u.x);
+    f[2] = E::lo(u.y); f[3] = E::hi(u.y);
+    f[4] = E::lo(u.z); f[5] = E::hi(u.z);
+    f[6] = E::lo(u.w); f[7] = E::hi(u.w);
 }
 
 __device__ __forceinline__ float warp_allmax(float x) {
@@ -632,7 +635,7 @@ __device__ __forceinline__ void load_block_ids(const StreamParams& p, int b, int
 // kPaged: keys come from the paged cache, per-request lengths, and cut units
 // leave their fragments in per-CTA slots (first segment of the CTA: slot 0,
 // last: slot 1).
-template <int D, int HC, bool kPaged>
+template <int D, int HC, bool kPaged, bool kF16 = false>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 decode_stream_kernel(const StreamParams p) {
     using L = StreamLayout<D, HC>;
@@ -750,7 +753,7 @@ decode_stream_kernel(const StreamParams p) {
 #pragma unroll
             for (int h = 0; h < HC; ++h) {
                 const uint16_t* qp = p.q + (static_cast<int64_t>(b) * p.Hq + hq0 + h) * D + sub * 8;
-                unpack8(*reinterpret_cast<const uint4*>(qp), qf[h]);
+                unpack8<kF16>(*reinterpret_cast<const uint4*>(qp), qf[h]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
             }
@@ -789,7 +792,7 @@ decode_stream_kernel(const StreamParams p) {
 #pragma unroll
                 for (int nn = 0; nn < kNK; ++nn) {
                     float kf[8];
-                    unpack8(kr[nn], kf);
+                    unpack8<kF16>(kr[nn], kf);
 #pragma unroll
                     for (int h = 0; h < HC; ++h) {
                         float sacc = 0.0f;
@@ -849,7 +852,7 @@ decode_stream_kernel(const StreamParams p) {
 #pragma unroll
                 for (int nn = 0; nn < kNK; ++nn) {
                     float vf[8];
-                    unpack8(vr[nn], vf);
+                    unpack8<kF16>(vr[nn], vf);
 #pragma unroll
                     for (int h = 0; h < HC; ++h) {
                         const float pw = pall[nn * HC + h];
@@ -917,7 +920,7 @@ decode_stream_kernel(const StreamParams p) {
                     const float lse2 = M + __log2f(Ls);
                     if (whole) {
                         const int64_t row = static_cast<int64_t>(b) * p.Hq + hq0 + h;
-                        const uint32_t pk = pack_bf16x2(out, 0.0f);
+                        const uint32_t pk = Elem16<kF16>::pack(out, 0.0f);
                         p.o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
                         if (d == 0 && p.lse != nullptr) p.lse[row] = lse2 * kLn2;
                     } else {
@@ -940,7 +943,7 @@ decode_stream_kernel(const StreamParams p) {
 
 // Merge the fragments of the units that slice boundaries cut; units a single
 // CTA covered were written directly.
-template <int D>
+template <int D, bool kF16 = false>
 __global__ void __launch_bounds__(D)
 decode_stream_combine_kernel(const StreamParams p, int hc) {
     const int row = blockIdx.x;
@@ -962,7 +965,7 @@ decode_stream_combine_kernel(const StreamParams p, int hc) {
         Ls += w;
         acc = fmaf(w, p.ws_o[slot * D + d], acc);
     }
-    const uint32_t pk = pack_bf16x2(acc / Ls, 0.0f);
+    const uint32_t pk = Elem16<kF16>::pack(acc / Ls, 0.0f);
     p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
 }
@@ -1057,7 +1060,7 @@ decode_paged_combine_kernel(const StreamParams p, int hc) {
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
 }
 
-template <int D, int HC, bool kPaged = false>
+template <int D, int HC, bool kPaged = false, bool kF16 = false>
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
     using L = StreamLayout<D, HC>;
     static bool attr_set[64] = {};
@@ -1065,22 +1068,22 @@ cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, HC, kPaged>,
+        cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, HC, kPaged, kF16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    decode_stream_kernel<D, HC, kPaged><<<grid, kStreamThreads, L::kBytes, st>>>(p);
+    decode_stream_kernel<D, HC, kPaged, kF16><<<grid, kStreamThreads, L::kBytes, st>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, bool kPaged = false>
+template <int D, bool kPaged = false, bool kF16 = false>
 cudaError_t launch_stream_d(const StreamParams& p, int hc, int grid, cudaStream_t st) {
     switch (hc) {
-        case 8: return launch_stream<D, 8, kPaged>(p, grid, st);
-        case 4: return launch_stream<D, 4, kPaged>(p, grid, st);
-        case 2: return launch_stream<D, 2, kPaged>(p, grid, st);
-        default: return launch_stream<D, 1, kPaged>(p, grid, st);
+        case 8: return launch_stream<D, 8, kPaged, kF16>(p, grid, st);
+        case 4: return launch_stream<D, 4, kPaged, kF16>(p, grid, st);
+        case 2: return launch_stream<D, 2, kPaged, kF16>(p, grid, st);
+        default: return launch_stream<D, 1, kPaged, kF16>(p, grid, st);
     }
 }
 
@@ -1178,15 +1181,26 @@ cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, cons
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.status = env.status;
     p.limit_ns = env.wait_limit_ns;
-    cudaError_t e = (s.D == 64) ? launch_stream_d<64>(p, g.hc, g.grid, env.stream)
-                                : launch_stream_d<128>(p, g.hc, g.grid, env.stream);
+    cudaError_t e;
+    if (s.f16)
+        e = (s.D == 64) ? launch_stream_d<64, false, true>(p, g.hc, g.grid, env.stream)
+                        : launch_stream_d<128, false, true>(p, g.hc, g.grid, env.stream);
+    else
+        e = (s.D == 64) ? launch_stream_d<64>(p, g.hc, g.grid, env.stream)
+                        : launch_stream_d<128>(p, g.hc, g.grid, env.stream);
     int launched = 1;
     if (e == cudaSuccess && g.nseg_max > 1) {
         const int rows = s.B * s.Hq;
-        if (s.D == 64)
+        if (s.f16) {
+            if (s.D == 64)
+                decode_stream_combine_kernel<64, true><<<rows, 64, 0, env.stream>>>(p, g.hc);
+            else
+                decode_stream_combine_kernel<128, true><<<rows, 128, 0, env.stream>>>(p, g.hc);
+        } else if (s.D == 64) {
             decode_stream_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, g.hc);
-        else
+        } else {
             decode_stream_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, g.hc);
+        }
         e = cudaGetLastError();
         launched = 2;
     }

@@ -244,10 +244,10 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t off16) {
 // S[tmem cols] = Q_tile . K_tile^T : M = 128, N = 128, K = D in steps of 16.
 // K step kk reads columns 16kk .. 16kk+15: 64-column box kk/4, 32 bytes
 // (kk%4) into each 128-byte row.  qd/kd: descriptors of the tiles' first box.
-template <int D>
+template <int D, bool kF16 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t kd,
                                          uint32_t leader) {
-    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false);
+    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, BN, false, false, kF16);
     constexpr int kSteps = D / 16;
     uint64_t a[kSteps], b[kSteps];
 #pragma unroll
@@ -265,10 +265,10 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t 
 // O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
 // P is read from tensor memory (8 columns per 16 keys); V is MN-major, K step
 // kk starts 16 key rows (2 KB) further.  vd: descriptor of the V tile.
-template <int D>
+template <int D, bool kF16 = false>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd,
                                          bool accumulate, uint32_t leader) {
-    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true);
+    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true, kF16);
     uint32_t a[BN / 16];
     uint64_t b[BN / 16];
 #pragma unroll
@@ -385,7 +385,7 @@ drain:
         wait_quiet(&bars->v_full[i % C::kVStages], (i / C::kVStages) & 1, kDrainLimitNs);
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kF16>
 __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const PrefillParams& p,
                            int n_items, const WaitGuard& g) {
     using C = Cfg<D>;
@@ -421,7 +421,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                 if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
                 if (j >= lo0 && j < n0) {
-                    issue_qk<D>(tmem + C::col_s(0), q_desc, k_desc, leader);
+                    issue_qk<D, kF16>(tmem + C::col_s(0), q_desc, k_desc, leader);
                     mma_commit(&bars->s_full[0], leader);
                 }
             }
@@ -433,7 +433,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                     !warp_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
                     goto drain;
                 tc_fence_after_sync();
-                issue_pv<D>(tmem + C::col_o(1), tmem + C::col_s(1),
+                issue_pv<D, kF16>(tmem + C::col_o(1), tmem + C::col_s(1),
                             desc_advance(v_desc0, pvs * kTile16), j - 1 > lo1, leader);
                 if (j - 1 == n1 - 1) {
                     mma_commit(&bars->o_full[1], leader);
@@ -443,7 +443,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
             if (j > lo0) mma_commit(&bars->v_empty[pvs], leader);
             if (j < nkv) {
                 if (j >= lo1 && j < n1) {
-                    issue_qk<D>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc,
+                    issue_qk<D, kF16>(tmem + C::col_s(1), desc_advance(q_desc, kTile16), k_desc,
                                 leader);
                     mma_commit(&bars->s_full[1], leader);
                 }
@@ -457,7 +457,8 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                         !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
-                    issue_pv<D>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > lo0, leader);
+                    issue_pv<D, kF16>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > lo0,
+                                      leader);
                     if (j == n0 - 1) {
                         mma_commit(&bars->o_full[0], leader);
                         ++o_cnt[0];
@@ -487,7 +488,7 @@ drain:
 // in .16x128b order (p[2n] row a, p[2n+1] row b, both P column 4n + i%4, i.e.
 // keys 8n + 2(i%4) and +1); se/sr receive this thread's exact and
 // bf16-rounded partial row sums.
-template <bool kPoly>
+template <bool kPoly, bool kF16>
 __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_log2,
                                           float neg_ma, float neg_mb, uint32_t (&p)[32],
                                           float (&se)[2], float (&sr)[2]) {
@@ -512,9 +513,9 @@ __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_l
                 e0 = ex2_approx(x0);
                 e1 = ex2_approx(x1);
             }
-            const uint32_t pk = pack_bf16x2(e0, e1);
+            const uint32_t pk = Elem16<kF16>::pack(e0, e1);
             acc_e[r][n & 1] = f2_add(acc_e[r][n & 1], f2_pack(e0, e1));
-            add_bf16x2_to_f32(pk, acc_r[r][0], acc_r[r][1]);
+            Elem16<kF16>::add2(pk, acc_r[r][0], acc_r[r][1]);
             p[2 * n + r] = pk;
         }
     }
@@ -553,7 +554,7 @@ struct RowState {
 
 // One S tile through the softmax: S -> P (bf16, in place in tensor memory),
 // sums and reference updated, O rescaled when the reference moves.
-template <int D>
+template <int D, bool kF16>
 __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint32_t o_addr,
                                              bool masked, int key0, int lim_a, int lim_b,
                                              int lft_a, int lft_b, bool first, float scale_log2) {
@@ -572,10 +573,10 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
     bool exact = first;
     if (!first) {
         if (masked)
-            tile_exp2<false>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+            tile_exp2<false, kF16>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
         else
-            tile_exp2<true>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
-        exact = !(se[0] <= 0x1p62f) || !(se[1] <= 0x1p62f);
+            tile_exp2<true, kF16>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+        exact = !(se[0] <= Elem16<kF16>::kMaxPartial) || !(se[1] <= Elem16<kF16>::kMaxPartial);
     }
     if (__any_sync(0xffffffffu, exact)) {
         // Exact path: row maximum (this thread's 32 keys, then the four
@@ -621,9 +622,9 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
         const float nma = (st.m[0] == -INFINITY) ? 0.0f : -st.m[0];
         const float nmb = (st.m[1] == -INFINITY) ? 0.0f : -st.m[1];
         if (masked)
-            tile_exp2<false>(s, scale_log2, nma, nmb, pk, se, sr);
+            tile_exp2<false, kF16>(s, scale_log2, nma, nmb, pk, se, sr);
         else
-            tile_exp2<true>(s, scale_log2, nma, nmb, pk, se, sr);
+            tile_exp2<true, kF16>(s, scale_log2, nma, nmb, pk, se, sr);
     }
     // P overwrites the first 64 columns of the tile (keys 2j, 2j+1 in column j).
     tmem_st_16x128b_x16(s_addr, pk);
@@ -638,7 +639,7 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
 // warp (lane quarter warp % 4, half (warp - 4) / 4), so every tile is worked
 // on by two warps per SM sub-partition.  Per key tile the tiles are taken in
 // the order the MMA warp produces them (S0 before S1).
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kF16>
 __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p, int n_items,
                               const WaitGuard& g) {
     using C = Cfg<D>;
@@ -688,7 +689,7 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                 ++s_cnt[t];
                 tc_fence_after_sync();
                 const int kbase = j * BN;
-                softmax_tile<D>(st[t], lanes + C::col_s(t), lanes + C::col_o(t),
+                softmax_tile<D, kF16>(st[t], lanes + C::col_s(t), lanes + C::col_o(t),
                                 kbase + BN - 1 > lim_first[t] || kbase < lft_last[t], kbase + kq,
                                 lim_a[t], lim_b[t], lft_a[t], lft_b[t], j == it.lo[t],
                                 p.scale_log2);
@@ -732,8 +733,9 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                         reinterpret_cast<uint32_t*>(p.o + orow * D + 64 * c + kq);
 #pragma unroll
                     for (int n = 0; n < 8; ++n)
-                        optr[4 * n] = pack_bf16x2(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
-                                                  __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
+                        optr[4 * n] =
+                            Elem16<kF16>::pack(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
+                                               __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
                 }
             }
             if ((lane & 3) == 0 && p.lse != nullptr) {
@@ -750,7 +752,7 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
     }
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -807,11 +809,11 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
         } else if (warp == 3) {
             if (lane == 0) producer_v<D, kPacked>(&tmV, smem, bars, p, n_items, g);
         } else if (warp == 1) {
-            mma_issuer<D, kPacked>(smem, bars, tmem, p, n_items, g);
+            mma_issuer<D, kPacked, kF16>(smem, bars, tmem, p, n_items, g);
         }
     } else {
         regs_increase<kSoftmaxRegs>();
-        softmax_group<D, kPacked>(bars, tmem, p, n_items, g);
+        softmax_group<D, kPacked, kF16>(bars, tmem, p, n_items, g);
     }
 
     tc_fence_before_sync();
@@ -954,7 +956,7 @@ __global__ void diag_wait_timeout_kernel(unsigned* status, unsigned long long li
     __syncthreads();
 }
 
-template <int D, bool kPacked>
+template <int D, bool kPacked, bool kF16 = false>
 cudaError_t launch_prefill_d(const PrefillMaps& maps, const PrefillParams& prm, int grid,
                              cudaStream_t stream) {
     using C = Cfg<D>;
@@ -963,13 +965,13 @@ cudaError_t launch_prefill_d(const PrefillMaps& maps, const PrefillParams& prm, 
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_bf16_kernel<D, kPacked>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_bf16_kernel<D, kPacked, kF16>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    prefill_bf16_kernel<D, kPacked>
+    prefill_bf16_kernel<D, kPacked, kF16>
         <<<grid, kThreads, C::kSmemBytes, stream>>>(maps.q, maps.k, maps.v, prm);
     return cudaGetLastError();
 }
@@ -1007,6 +1009,9 @@ cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse
     if (grid_out) *grid_out = grid;
     if (items_out) *items_out = prm.n_items;
     if (kernels_launched) *kernels_launched = 1;
+    if (s.f16)
+        return (s.D == 64) ? launch_prefill_d<64, false, true>(maps, prm, grid, env.stream)
+                           : launch_prefill_d<128, false, true>(maps, prm, grid, env.stream);
     return (s.D == 64) ? launch_prefill_d<64, false>(maps, prm, grid, env.stream)
                        : launch_prefill_d<128, false>(maps, prm, grid, env.stream);
 }

@@ -331,13 +331,14 @@ __device__ __forceinline__ void tmem_wait_st() {
 // ---------------------------------------------------------------------------
 // tcgen05.mma descriptors
 // ---------------------------------------------------------------------------
-// Instruction descriptor, kind::f16 with bf16 A/B and an fp32 accumulator:
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format
-//   (1 = bf16), 15 A major (0 = K-major, 1 = MN-major), 16 B major,
+// Instruction descriptor, kind::f16 with bf16 (or, with f16, fp16) A/B and an
+// fp32 accumulator:
+//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16, 0 = f16), 10-12 B
+//   format (same), 15 A major (0 = K-major, 1 = MN-major), 16 B major,
 //   17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t mma_idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                          bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) |
+                                                          bool b_mn_major, bool f16 = false) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
            (static_cast<uint32_t>(a_mn_major) << 15) |
            (static_cast<uint32_t>(b_mn_major) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) |
@@ -539,5 +540,58 @@ __device__ __forceinline__ void exp2_poly_x2(uint64_t x2, float& y0, float& y1) 
 
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// fp16 counterparts: two floats -> packed f16x2 (round to nearest even, lo in
+// the low half), the halves of a pair -> fp32 (exact), and the mixed-precision
+// add of both halves to two fp32 accumulators.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t x) {
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(f) : "r"(x));
+    return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t x) {
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}"
+        : "=f"(f) : "r"(x));
+    return f;
+}
+__device__ __forceinline__ void add_f16x2_to_f32(uint32_t pk, float& lo_acc, float& hi_acc) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\t"
+        "add.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(lo_acc), "+f"(hi_acc) : "r"(pk));
+}
+
+// The 16-bit I/O element: bf16 (kF16 = false) or fp16.  kMaxPartial bounds a
+// thread's partial weight sum on the prefill's fast path so that every weight
+// stays finite in the element type: 2^62 for bf16 (fp32's exponent range),
+// 2^15 for fp16 (largest finite value 65504).
+template <bool kF16>
+struct Elem16 {
+    static constexpr float kMaxPartial = kF16 ? 0x1p15f : 0x1p62f;
+    __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+        if constexpr (kF16) return pack_f16x2(lo, hi);
+        else return pack_bf16x2(lo, hi);
+    }
+    __device__ static __forceinline__ void add2(uint32_t pk, float& lo_acc, float& hi_acc) {
+        if constexpr (kF16) add_f16x2_to_f32(pk, lo_acc, hi_acc);
+        else add_bf16x2_to_f32(pk, lo_acc, hi_acc);
+    }
+    __device__ static __forceinline__ float lo(uint32_t x) {
+        if constexpr (kF16) return f16_lo_to_f32(x);
+        else return bf16_lo_to_f32(x);
+    }
+    __device__ static __forceinline__ float hi(uint32_t x) {
+        if constexpr (kF16) return f16_hi_to_f32(x);
+        else return bf16_hi_to_f32(x);
+    }
+};
 
 }  // namespace attn

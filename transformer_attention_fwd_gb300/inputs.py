@@ -76,6 +76,8 @@ def torch_dtype(dtype: str) -> torch.dtype:
         return torch.float32
     if dtype == "bf16":
         return torch.bfloat16
+    if dtype == "f16":
+        return torch.float16
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
@@ -84,8 +86,8 @@ def make_qkv(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, D: int,
     """Draw Q [B,Hq,Tq,D], K and V [B,Hkv,Tk,D] iid N(0,1) on the CPU.
 
     One ``torch.Generator`` seeded with ``seed`` draws Q, then K, then V in
-    float32; bf16 workloads then round each tensor to bf16 (RNE).  Returns CPU
-    tensors in the I/O dtype.
+    float32; bf16 (fp16) workloads then round each tensor to bf16 (fp16), RNE.
+    Returns CPU tensors in the I/O dtype.
     """
     g = torch.Generator().manual_seed(int(seed))
     q = torch.randn(B, Hq, Tq, D, generator=g, dtype=torch.float32)
