@@ -530,19 +530,26 @@ __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_l
 }
 
 // On a tile that straddles the diagonal or the end of the keys, keys past a
-// row's last visible key become -inf; with a sliding window, so do keys before
-// the row's first visible key ("Attention 入门" §11.8.4, only the most recent
-// W tokens).
-__device__ __forceinline__ void mask_tile(uint32_t (&s)[64], int key0, int lim_a, int lim_b,
-                                          int lft_a, int lft_b) {
+// row's last visible key become -inf.  A thread's element (n, k) holds key
+// key0 + 8n + (k & 1); dr = last visible key - key0 of its rows a (k < 2) and
+// b, so each test compares a compile-time offset with one register.
+__device__ __forceinline__ void mask_right(uint32_t (&s)[64], int dr_a, int dr_b) {
 #pragma unroll
     for (int n = 0; n < 16; ++n)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int key = key0 + 8 * n + (k & 1);
-            if (key > ((k < 2) ? lim_a : lim_b) || key < ((k < 2) ? lft_a : lft_b))
-                s[4 * n + k] = __float_as_uint(-INFINITY);
-        }
+        for (int k = 0; k < 4; ++k)
+            if (8 * n + (k & 1) > ((k < 2) ? dr_a : dr_b)) s[4 * n + k] = __float_as_uint(-INFINITY);
+}
+
+// With a sliding window ("Attention 入门" §11.8.4, only the most recent W
+// tokens), keys before a row's first visible key become -inf too (dl = first
+// visible key - key0).
+__device__ __forceinline__ void mask_left(uint32_t (&s)[64], int dl_a, int dl_b) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (8 * n + (k & 1) < ((k < 2) ? dl_a : dl_b)) s[4 * n + k] = __float_as_uint(-INFINITY);
 }
 
 // Per-thread softmax state of one query tile: running reference m (log2
@@ -554,14 +561,18 @@ struct RowState {
 
 // One S tile through the softmax: S -> P (bf16, in place in tensor memory),
 // sums and reference updated, O rescaled when the reference moves.
+// mask_r / mask_l: the tile crosses some row's last / first visible key.
 template <int D, bool kF16>
 __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint32_t o_addr,
-                                             bool masked, int key0, int lim_a, int lim_b,
-                                             int lft_a, int lft_b, bool first, float scale_log2) {
+                                             bool mask_r, bool mask_l, int key0, int lim_a,
+                                             int lim_b, int lft_a, int lft_b, bool first,
+                                             float scale_log2) {
     uint32_t s[64];
     tmem_ld_16x256b_x16(s_addr, s);
     tmem_wait_ld64(s);
-    if (masked) mask_tile(s, key0, lim_a, lim_b, lft_a, lft_b);
+    if (mask_r) mask_right(s, lim_a - key0, lim_b - key0);
+    if (mask_l) mask_left(s, lft_a - key0, lft_b - key0);
+    const bool masked = mask_r || mask_l;
     // Fast path: weights against the running reference without a row
     // maximum.  bf16 P and the fp32 sums and accumulators have fp32's
     // exponent range, so weights far above 1 lose no relative precision; a
@@ -690,9 +701,9 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                 tc_fence_after_sync();
                 const int kbase = j * BN;
                 softmax_tile<D, kF16>(st[t], lanes + C::col_s(t), lanes + C::col_o(t),
-                                kbase + BN - 1 > lim_first[t] || kbase < lft_last[t], kbase + kq,
-                                lim_a[t], lim_b[t], lft_a[t], lft_b[t], j == it.lo[t],
-                                p.scale_log2);
+                                      kbase + BN - 1 > lim_first[t], kbase < lft_last[t],
+                                      kbase + kq, lim_a[t], lim_b[t], lft_a[t], lft_b[t],
+                                      j == it.lo[t], p.scale_log2);
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(&bars->p_full[t]);
