@@ -165,14 +165,15 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v,
                             attn_dtype dtype, cudaStream_t stream);
 
 /*
- * attn_fwd_varlen -- bf16 attention over variable-length sequences packed
+ * attn_fwd_varlen -- attention over variable-length sequences packed
  * back to back along the token axis, in the (T, H, D) layout of "第 11 章 ·
  * Attention 入门", 11.11.  Each sequence is its own attention problem: with
  * causal = 1 its query rows are aligned to the end of its keys (a chunk of
  * new tokens against a longer history, §11.8.2), and window > 0 adds the
  * sliding window of attn_fwd_window (§11.8.4).
- *   q, o:   [total_q, Hq, D] bf16, 16-byte aligned.
- *   k, v:   [total_k, Hkv, D] bf16, 16-byte aligned.
+ *   q, o:   [total_q, Hq, D] bf16 or fp16 (dtype ATTN_BF16 / ATTN_F16; ATTN_F32
+ *           returns ATTN_ERR_UNSUPPORTED), 16-byte aligned.
+ *   k, v:   [total_k, Hkv, D] in the same type, 16-byte aligned.
  *   cu_seqlens_q, cu_seqlens_k: [B + 1] int32, device.  Sequence b owns
  *           query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
  *           cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1.
@@ -196,7 +197,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
                             void* o, float* lse, const int* cu_seqlens_q,
                             const int* cu_seqlens_k, int B, int Hq, int Hkv,
                             int total_q, int total_k, int D, int causal,
-                            int window, float scale, cudaStream_t stream);
+                            int window, float scale, attn_dtype dtype,
+                            cudaStream_t stream);
 
 /*
  * attn_fwd_decode_paged -- decode (one query row per (b, hq)) against a paged
@@ -205,9 +207,10 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v,
  * and the V rows of its tokens for every KV head, and block_table[req][t / 16]
  * names the block of token t of request req; 16 is that passage's page size,
  * any page_size >= 1 is accepted here).
- *   q, o:        [B, Hq, 1, D] bf16, 16-byte aligned.
- *   kv_cache:    [num_blocks, 2, Hkv, page_size, D] bf16 (index 0 of the second
- *                dimension = K, 1 = V), 16-byte aligned.
+ *   q, o:        [B, Hq, 1, D] bf16 or fp16 (dtype ATTN_BF16 / ATTN_F16;
+ *                ATTN_F32 returns ATTN_ERR_UNSUPPORTED), 16-byte aligned.
+ *   kv_cache:    [num_blocks, 2, Hkv, page_size, D] in the same type (index 0
+ *                of the second dimension = K, 1 = V), 16-byte aligned.
  *   block_table: [B, max_pages_per_seq] int32, device; entry [b][p] is the
  *                block holding tokens p*page_size .. p*page_size+page_size-1 of
  *                request b.  Entries past a request's last page are not read.
@@ -231,7 +234,7 @@ attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache,
                                   const int* block_table, const int* seq_lens,
                                   void* o, float* lse, int B, int Hq, int Hkv,
                                   int D, int page_size, int max_pages_per_seq,
-                                  int num_blocks, float scale,
+                                  int num_blocks, float scale, attn_dtype dtype,
                                   cudaStream_t stream);
 
 /*

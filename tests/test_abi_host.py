@@ -96,10 +96,11 @@ def test_decode_split_count_range(lib):
 def test_paged_decode_arguments_rejected_before_launch(lib, args, code, msg):
     f = lib.attn_fwd_decode_paged
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
     f.restype = ctypes.c_int
     lib.attn_last_error.restype = ctypes.c_char_p
-    assert f(*args, None) == code
+    assert f(*args, 1, None) == code  # bf16
+    assert f(*args, 2, None) == code  # fp16: the same checks
     assert msg in lib.attn_last_error().decode()
 
 
@@ -121,14 +122,14 @@ def test_window_arguments_rejected_before_launch(lib):
 def test_varlen_arguments_rejected_before_launch(lib):
     f = lib.attn_fwd_varlen
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    f.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P]
+    f.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P]
     f.restype = ctypes.c_int
     lib.attn_last_error.restype = ctypes.c_char_p
 
     def call(q=FAKE, cu=FAKE, B=2, Hq=4, Hkv=2, tq=300, tk=300, D=128, causal=1, window=0,
-             scale=0.1):
+             scale=0.1, dtype=1):
         return f(q, FAKE, FAKE, FAKE, None, cu, FAKE, B, Hq, Hkv, tq, tk, D, causal, window,
-                 scale, None)
+                 scale, dtype, None)
 
     assert call(causal=0, window=16) == 1 and b"causal" in lib.attn_last_error()
     assert call(window=-1) == 1
@@ -138,6 +139,9 @@ def test_varlen_arguments_rejected_before_launch(lib):
     assert call(scale=0.0) == 1
     assert call(q=FAKE + 4) == 1
     assert call(cu=None) == 1
+    assert call(dtype=0) == 2  # fp32 is not packed
+    assert call(dtype=5) == 1
+    assert call(D=96, dtype=2) == 2
     assert call(B=0) == 1
     # No query rows: nothing to launch, no device needed.
     assert call(q=None, tq=0) == 0

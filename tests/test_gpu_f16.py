@@ -100,3 +100,33 @@ def test_f16_is_more_precise_than_bf16():
     eb = np.abs(ob.float().cpu().numpy() - o_ref).max()
     eh = np.abs(oh.float().cpu().numpy() - o_ref).max()
     assert eh <= eb, (eh, eb)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_f16_varlen_matches_oracle(causal):
+    from transformer_attention_fwd_gb300.inputs import make_varlen
+    a = attn()
+    lq, lk = [1, 127, 300, 0, 700], [1, 127, 600, 5, 700]
+    if not causal:
+        lk = lq[:3] + [5, 700]
+    q, k, v, cq, ck = make_varlen(lq, lk, 8, 2, 128, seed=107, dtype="f16")
+    o, lse = a.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), causal)
+    check_status(a)
+    assert o.dtype == torch.float16
+    o_ref, lse_ref = oracle.attention_varlen_f64(q, k, v, cq, ck, causal)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= TOL_O_F16
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= TOL_LSE_F16
+
+
+def test_f16_paged_decode_matches_oracle():
+    from transformer_attention_fwd_gb300.inputs import make_paged
+    a = attn()
+    q, kv, bt, sl = make_paged(5, 16, 4, 128, 16, [1000, 1, 0, 77, 2048], seed=108, dtype="f16")
+    o, lse = a.attn_fwd_decode_paged(*to_dev(q, kv, bt, sl))
+    check_status(a)
+    assert o.dtype == torch.float16
+    o_ref, lse_ref = oracle.decode_paged_f64(q, kv, bt, sl)
+    o_g = o.float().cpu().numpy()[:, :, 0, :]
+    assert np.abs(o_g - o_ref).max() <= TOL_O_F16
+    l_g, fin = lse.cpu().numpy(), np.isfinite(lse_ref)
+    assert (np.isfinite(l_g) == fin).all() and np.abs(l_g[fin] - lse_ref[fin]).max() <= TOL_LSE_F16

@@ -52,9 +52,9 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         "attn_fwd": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "attn_fwd_prefill": [P, P, P, P, P, I, I, I, I, I, I, I, F, P],
         "attn_fwd_decode": [P, P, P, P, P, I, I, I, I, I, F, I, P],
-        "attn_fwd_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P],
+        "attn_fwd_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "attn_fwd_window": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
-        "attn_fwd_varlen": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P],
+        "attn_fwd_varlen": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P],
         "attn_get_device_status": [P],
         "attn_diag_mma_tile": [P, P, P, P, P, I, P],
         "attn_diag_wait_timeout": [LL, P],
@@ -210,8 +210,8 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, window: i
             raise ValueError(f"{name} must be contiguous")
     if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or q.shape[2] != k.shape[2]:
         raise ValueError("q must be [total_q, Hq, D] and k, v [total_k, Hkv, D]")
-    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
-        raise ValueError("attn_fwd_varlen takes bf16 tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("attn_fwd_varlen takes bf16 or fp16 tensors")
     if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must be int32")
     if (cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape
@@ -226,7 +226,9 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, window: i
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
     _check(lib.attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens_q),
                                _ptr(cu_seqlens_k), B, Hq, Hkv, total_q, total_k, D,
-                               1 if causal else 0, int(window), scale, _stream_handle(stream)))
+                               1 if causal else 0, int(window), scale,
+                               ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16,
+                               _stream_handle(stream)))
     return o, lse
 
 
@@ -244,10 +246,10 @@ def attn_fwd_decode_paged(q, kv_cache, block_table, seq_lens, scale: float | Non
             raise ValueError(f"{name} must be a CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    if q.dim() != 4 or q.shape[2] != 1 or q.dtype != torch.bfloat16:
-        raise ValueError("q must be bf16 [B, Hq, 1, D]")
-    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.dtype != torch.bfloat16:
-        raise ValueError("kv_cache must be bf16 [num_blocks, 2, Hkv, page_size, D]")
+    if q.dim() != 4 or q.shape[2] != 1 or q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q must be bf16 or fp16 [B, Hq, 1, D]")
+    if kv_cache.dim() != 5 or kv_cache.shape[1] != 2 or kv_cache.dtype != q.dtype:
+        raise ValueError("kv_cache must be [num_blocks, 2, Hkv, page_size, D] in q's dtype")
     if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise ValueError("block_table and seq_lens must be int32")
     B, Hq, _, D = q.shape
@@ -260,7 +262,9 @@ def attn_fwd_decode_paged(q, kv_cache, block_table, seq_lens, scale: float | Non
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     _check(lib.attn_fwd_decode_paged(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
                                      _ptr(o), _ptr(lse), B, Hq, Hkv, D, page,
-                                     block_table.shape[1], nblk, scale, _stream_handle(stream)))
+                                     block_table.shape[1], nblk, scale,
+                                     ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16,
+                                     _stream_handle(stream)))
     return o, lse
 
 

@@ -384,7 +384,11 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq,
                             int Hkv, int total_q, int total_k, int D, int causal, int window,
-                            float scale, cudaStream_t stream) {
+                            float scale, attn_dtype dtype, cudaStream_t stream) {
+    if (dtype == ATTN_F32)
+        return fail(ATTN_ERR_UNSUPPORTED, "packed sequences are implemented for 16-bit I/O only");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
     if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || total_q < 0 || total_k < 0)
         return fail(ATTN_ERR_INVALID_ARG,
                     "B, Hq, Hkv, D must be >= 1 and total_q, total_k >= 0 (got %d, %d, %d, %d, %d, %d)",
@@ -408,7 +412,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
         return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
     if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4)))
         return fail(ATTN_ERR_INVALID_ARG, "cu_seqlens_q, cu_seqlens_k and lse must be 4-byte aligned");
-    const VarlenShape s{B, Hq, Hkv, total_q, total_k, D, causal ? 1 : 0, window, scale};
+    VarlenShape s{B, Hq, Hkv, total_q, total_k, D, causal ? 1 : 0, window, scale};
+    s.f16 = dtype == ATTN_F16 ? 1 : 0;
     const size_t bytes = varlen_workspace_bytes(s);
     if (bytes == 0)
         return fail(ATTN_ERR_INVALID_ARG, "too many work items (Hq * query blocks must fit in 31 bits)");
@@ -418,9 +423,10 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     PrefillMaps maps;
     const int box = prefill_box_rows();
     if (total_k > 0) {
-        if ((st = make_map(q, total_q, Hq, D, box, 3, &maps.q, true)) != ATTN_OK) return st;
-        if ((st = make_map(k, total_k, Hkv, D, box, 3, &maps.k, true)) != ATTN_OK) return st;
-        if ((st = make_map(v, total_k, Hkv, D, box, 3, &maps.v, true)) != ATTN_OK) return st;
+        const bool f16 = s.f16 != 0;
+        if ((st = make_map(q, total_q, Hq, D, box, 3, &maps.q, true, f16)) != ATTN_OK) return st;
+        if ((st = make_map(k, total_k, Hkv, D, box, 3, &maps.k, true, f16)) != ATTN_OK) return st;
+        if ((st = make_map(v, total_k, Hkv, D, box, 3, &maps.v, true, f16)) != ATTN_OK) return st;
     }
     void* ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
@@ -448,7 +454,11 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
 attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache, const int* block_table,
                                   const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv,
                                   int D, int page_size, int max_pages_per_seq, int num_blocks,
-                                  float scale, cudaStream_t stream) {
+                                  float scale, attn_dtype dtype, cudaStream_t stream) {
+    if (dtype == ATTN_F32)
+        return fail(ATTN_ERR_UNSUPPORTED, "the paged decode is implemented for 16-bit I/O only");
+    if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
     if (!q || !kv_cache || !block_table || !seq_lens || !o)
         return fail(ATTN_ERR_INVALID_ARG, "q, kv_cache, block_table, seq_lens and o must be non-null");
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(o, 16))
@@ -471,7 +481,8 @@ attn_status attn_fwd_decode_paged(const void* q, const void* kv_cache, const int
     LaunchEnv env;
     attn_status st = device_env(stream, &env);
     if (st != ATTN_OK) return st;
-    const PagedShape s{B, Hq, Hkv, D, page_size, max_pages_per_seq, num_blocks, scale};
+    PagedShape s{B, Hq, Hkv, D, page_size, max_pages_per_seq, num_blocks, scale};
+    s.f16 = dtype == ATTN_F16 ? 1 : 0;
     const size_t bytes = decode_paged_workspace_bytes(s, env.num_sms);
     void* ws = nullptr;
     cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);

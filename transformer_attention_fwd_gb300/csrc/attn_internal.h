@@ -50,6 +50,7 @@ struct VarlenShape {
     int causal;
     int window;  // > 0: sliding window (causal only)
     float scale;
+    int f16 = 0;  // fp16 q, k, v and o instead of bf16
 };
 // One work item of the packed prefill: {q0, Tq, k0, Tk}, {query block, head, 0, 0}.
 struct VarlenSchedule {
@@ -96,6 +97,7 @@ struct PagedShape {
     int B, Hq, Hkv, D;
     int page, max_pages, num_blocks;
     float scale;
+    int f16 = 0;  // fp16 q, cache and o instead of bf16
 };
 size_t decode_paged_workspace_bytes(const PagedShape& s, int num_sms);
 cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,

@@ -1024,7 +1024,7 @@ paged_prefix_kernel(const int32_t* seq_lens, int B, int max_keys, long long unit
 
 // Paged mode: merge the fragments of cut units (CTA slots) and give requests
 // without keys O = 0, lse = -inf; units one CTA covered were written directly.
-template <int D>
+template <int D, bool kF16 = false>
 __global__ void __launch_bounds__(D)
 decode_paged_combine_kernel(const StreamParams p, int hc) {
     const int row = blockIdx.x;
@@ -1055,7 +1055,7 @@ decode_paged_combine_kernel(const StreamParams p, int hc) {
         Ls += w;
         acc = fmaf(w, p.ws_o[slot * D + d], acc);
     }
-    const uint32_t pk = pack_bf16x2(acc / Ls, 0.0f);
+    const uint32_t pk = Elem16<kF16>::pack(acc / Ls, 0.0f);
     p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
 }
@@ -1149,15 +1149,26 @@ cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
     paged_prefix_kernel<<<1, 1024, 0, env.stream>>>(seq_lens, s.B, s.max_pages * s.page,
                                                     units_per_req, grid, cum, geom, env.status);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess)
-        e = (s.D == 64) ? launch_stream_d<64, true>(p, hc, grid, env.stream)
-                        : launch_stream_d<128, true>(p, hc, grid, env.stream);
+    if (e == cudaSuccess) {
+        if (s.f16)
+            e = (s.D == 64) ? launch_stream_d<64, true, true>(p, hc, grid, env.stream)
+                            : launch_stream_d<128, true, true>(p, hc, grid, env.stream);
+        else
+            e = (s.D == 64) ? launch_stream_d<64, true>(p, hc, grid, env.stream)
+                            : launch_stream_d<128, true>(p, hc, grid, env.stream);
+    }
     if (e == cudaSuccess) {
         const int rows = s.B * s.Hq;
-        if (s.D == 64)
+        if (s.f16) {
+            if (s.D == 64)
+                decode_paged_combine_kernel<64, true><<<rows, 64, 0, env.stream>>>(p, hc);
+            else
+                decode_paged_combine_kernel<128, true><<<rows, 128, 0, env.stream>>>(p, hc);
+        } else if (s.D == 64) {
             decode_paged_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, hc);
-        else
+        } else {
             decode_paged_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, hc);
+        }
         e = cudaGetLastError();
     }
     if (grid_out) *grid_out = grid;

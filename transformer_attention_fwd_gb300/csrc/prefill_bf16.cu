@@ -1057,6 +1057,9 @@ cudaError_t launch_prefill_packed_bf16(const PrefillMaps& maps, uint16_t* o, flo
         return cudaSuccess;
     }
     if (kernels_launched) *kernels_launched = 1;
+    if (s.f16)
+        return (s.D == 64) ? launch_prefill_d<64, true, true>(maps, prm, grid, env.stream)
+                           : launch_prefill_d<128, true, true>(maps, prm, grid, env.stream);
     return (s.D == 64) ? launch_prefill_d<64, true>(maps, prm, grid, env.stream)
                        : launch_prefill_d<128, true>(maps, prm, grid, env.stream);
 }

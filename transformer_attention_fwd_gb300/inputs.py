@@ -131,11 +131,11 @@ PAGED_WORKLOADS = {
 
 
 def make_paged(B: int, Hq: int, Hkv: int, D: int, page: int, seq_lens, seed: int = 0,
-               spare_blocks: int = 3, max_pages: int | None = None):
+               spare_blocks: int = 3, max_pages: int | None = None, dtype: str = "bf16"):
     """Draw a paged-cache decode problem on the CPU.
 
     q [B, Hq, 1, D] and the block pool kv [num_blocks, 2, Hkv, page, D] are iid
-    N(0, 1) rounded to bf16; the pool has the blocks the requests need plus
+    N(0, 1) rounded to bf16 (or fp16 with dtype="f16"); the pool has the blocks the requests need plus
     `spare_blocks` unreferenced ones.  Request b's pages get distinct blocks in
     a seeded random order; block-table entries past a request's last page are
     -1 (never valid).  Returns (q, kv, block_table int32 [B, max_pages],
@@ -147,8 +147,9 @@ def make_paged(B: int, Hq: int, Hkv: int, D: int, page: int, seq_lens, seed: int
     if max_pages is None:
         max_pages = max(1, max(pages))
     nblk = sum(pages) + spare_blocks
-    q = torch.randn(B, Hq, 1, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    kv = torch.randn(nblk, 2, Hkv, page, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    td = torch_dtype(dtype)
+    q = torch.randn(B, Hq, 1, D, generator=g, dtype=torch.float32).to(td)
+    kv = torch.randn(nblk, 2, Hkv, page, D, generator=g, dtype=torch.float32).to(td)
     perm = torch.randperm(nblk, generator=g)
     table = torch.full((B, max_pages), -1, dtype=torch.int32)
     nxt = 0
@@ -199,9 +200,10 @@ VARLEN_WORKLOADS = {
 }
 
 
-def make_varlen(seqlens_q, seqlens_k, Hq: int, Hkv: int, D: int, seed: int = 0):
+def make_varlen(seqlens_q, seqlens_k, Hq: int, Hkv: int, D: int, seed: int = 0,
+                dtype: str = "bf16"):
     """Draw a packed variable-length problem on the CPU: q [sum Tq, Hq, D],
-    k and v [sum Tk, Hkv, D], iid N(0, 1) rounded to bf16, and the int32
+    k and v [sum Tk, Hkv, D], iid N(0, 1) rounded to bf16 (or fp16), and the int32
     offsets cu_seqlens_q, cu_seqlens_k [B + 1] (sequence b at rows cu[b] ..
     cu[b+1]-1)."""
     g = torch.Generator().manual_seed(int(seed))
@@ -210,9 +212,10 @@ def make_varlen(seqlens_q, seqlens_k, Hq: int, Hkv: int, D: int, seed: int = 0):
     if len(lq) != len(lk):
         raise ValueError("seqlens_q and seqlens_k differ in length")
     tq, tk = sum(lq), sum(lk)
-    q = torch.randn(tq, Hq, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    k = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    v = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    td = torch_dtype(dtype)
+    q = torch.randn(tq, Hq, D, generator=g, dtype=torch.float32).to(td)
+    k = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(td)
+    v = torch.randn(tk, Hkv, D, generator=g, dtype=torch.float32).to(td)
     cq = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
     ck = torch.tensor([0] + lk, dtype=torch.int64).cumsum(0).to(torch.int32)
     return q, k, v, cq, ck
