@@ -79,6 +79,27 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o,
                      cudaStream_t stream);
 
 /*
+ * attn_fwd_host -- attn_fwd on HOST buffers: q, k, v are read from host
+ * memory and o, lse are written back to host memory; the call enqueues the
+ * copies and the compute on `stream` and returns (the outputs are in place
+ * once `stream` has completed the call).  Arguments, layouts and errors are
+ * those of attn_fwd, with host pointers (16-byte aligned; page-locked memory,
+ * cudaMallocHost or cudaHostRegister, lets the copies overlap the compute,
+ * pageable memory works but serialises them).
+ * The (b, hkv) pairs are cut into up to four contiguous chunks; each chunk is
+ * copied in on one copy stream, computed on `stream` (as attn_fwd with B =
+ * its pairs, Hq = Hq / Hkv, Hkv = 1) and copied out on another, so the copies
+ * of one chunk overlap the compute of its neighbours.  Device buffers for the
+ * five tensors are allocated and freed stream-ordered on `stream`
+ * (ATTN_ERR_NO_MEMORY if that fails).  The two copy streams are shared by all
+ * calls on one device.
+ */
+attn_status attn_fwd_host(const void* q, const void* k, const void* v,
+                          void* o, float* lse, int B, int Hq, int Hkv, int Tq,
+                          int Tk, int D, int causal, float scale,
+                          attn_dtype dtype, cudaStream_t stream);
+
+/*
  * attn_fwd_prefill -- bf16 tiled attention on the 5th-generation tensor cores
  * ("Self-Attention机制深入理解" §12.2 tiling with §12.3 online softmax; causal
  * tiles wholly above the diagonal are skipped and the diagonal tile is masked

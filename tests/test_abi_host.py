@@ -29,7 +29,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_prefill", "attn_fwd_decode", "attn_fwd_decode_paged",
-            "attn_fwd_window", "attn_fwd_varlen",
+            "attn_fwd_window", "attn_fwd_varlen", "attn_fwd_host",
             "attn_get_device_status", "attn_last_error", "attn_diag_mma_tile",
             "attn_diag_wait_timeout"} <= set(names)
     for n in names:
@@ -102,6 +102,19 @@ def test_paged_decode_arguments_rejected_before_launch(lib, args, code, msg):
     assert f(*args, 1, None) == code  # bf16
     assert f(*args, 2, None) == code  # fp16: the same checks
     assert msg in lib.attn_last_error().decode()
+
+
+def test_host_call_arguments_rejected_before_launch(lib):
+    f = lib.attn_fwd_host
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
+    f.restype = ctypes.c_int
+    lib.attn_last_error.restype = ctypes.c_char_p
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 1, 0.1, 9, None) == 1  # dtype
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 96, 1, 0.1, 1, None) == 2   # D
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 3, 64, 64, 128, 1, 0.1, 1, None) == 1  # GQA
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 2, 80, 64, 128, 1, 0.1, 2, None) == 1  # Tq > Tk
+    assert f(None, FAKE, FAKE, FAKE, None, 1, 4, 2, 64, 64, 128, 1, 0.1, 1, None) == 1
 
 
 def test_window_arguments_rejected_before_launch(lib):

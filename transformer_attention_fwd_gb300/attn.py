@@ -54,6 +54,7 @@ def _load(path: str = LIB_PATH) -> ctypes.CDLL:
         "attn_fwd_decode": [P, P, P, P, P, I, I, I, I, I, F, I, P],
         "attn_fwd_decode_paged": [P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "attn_fwd_window": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
+        "attn_fwd_host": [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P],
         "attn_fwd_varlen": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P],
         "attn_get_device_status": [P],
         "attn_diag_mma_tile": [P, P, P, P, P, I, P],
@@ -145,6 +146,36 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     o, lse = _outputs(q, out, lse, want_lse)
     _check(lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk, D,
                         1 if causal else 0, scale, dt, _stream_handle(stream)))
+    return o, lse
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+                  lse=None, want_lse: bool = True, stream=None):
+    """``attn_fwd`` on host tensors (``attn_fwd_host``): q [B, Hq, Tq, D] and
+    k/v [B, Hkv, Tk, D] CPU tensors (fp32, bf16 or fp16; pinned memory lets
+    the copies overlap the compute).  Returns CPU ``(o, lse)``, complete once
+    ``stream`` (default: the current CUDA stream) has run the call."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+        if not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be contiguous [B, H, T, D]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+    dt = {torch.float32: ATTN_F32, torch.bfloat16: ATTN_BF16, torch.float16: ATTN_F16}.get(q.dtype)
+    if dt is None:
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    B, Hq, Tq, D = q.shape
+    Bk, Hkv, Tk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
+        raise ValueError("k and v must be [B, Hkv, Tk, D] with q's B and D")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    pin = q.is_pinned()
+    o = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, pin_memory=pin)
+    _check(lib.attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Tq, Tk,
+                             D, 1 if causal else 0, scale, dt, _stream_handle(stream)))
     return o, lse
 
 

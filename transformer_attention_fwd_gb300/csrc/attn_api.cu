@@ -52,6 +52,7 @@ struct DeviceState {
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned* status = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr;  // attn_fwd_host's copy streams
 };
 std::mutex g_dev_mutex;
 DeviceState g_dev[64];
@@ -302,6 +303,32 @@ attn_status run_decode(const void* q, const void* k, const void* v, void* o, flo
     return ok();
 }
 
+// attn_fwd's dispatch after validation: fp32 -> CUDA-core kernel; 16-bit
+// Tq = 1 -> stream-K decode; otherwise the tensor-core prefill.
+attn_status dispatch(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const Shape& s, attn_dtype dtype, const LaunchEnv& env) {
+    if (dtype == ATTN_F32) {
+        int kernels = 0;
+        cudaError_t e = launch_simt_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse,
+                                        s, env, &kernels);
+        if (e == cudaErrorInvalidConfiguration)
+            return fail(ATTN_ERR_UNSUPPORTED, "Tq=%d too long for the fp32 kernel's grid", s.Tq);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 launch");
+        record_launch(s.B * s.Hq, (s.Tq + 15) / 16, kernels);
+        return ok();
+    }
+    if (s.Tq == 1) return run_decode(q, k, v, o, lse, s, 0, env);
+    return run_prefill(q, k, v, o, lse, s, env);
+}
+
+// attn_fwd_host's pipeline depth: the problem is cut into at most this many
+// chunks of (b, hkv) units.
+#ifndef ATTN_HOST_CHUNKS
+#define ATTN_HOST_CHUNKS 4
+#endif
+constexpr int kHostChunks = ATTN_HOST_CHUNKS;
+
 }  // namespace
 }  // namespace attn
 
@@ -347,19 +374,128 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     if (st != ATTN_OK) return st;
     Shape s{B, Hq, Hkv, Tq, Tk, D, causal ? 1 : 0, scale};
     s.f16 = dtype == ATTN_F16 ? 1 : 0;
-    if (dtype == ATTN_F32) {
-        int kernels = 0;
-        cudaError_t e = launch_simt_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                        static_cast<const float*>(v), static_cast<float*>(o), lse,
-                                        s, env, &kernels);
-        if (e == cudaErrorInvalidConfiguration)
-            return fail(ATTN_ERR_UNSUPPORTED, "Tq=%d too long for the fp32 kernel's grid", Tq);
-        if (e != cudaSuccess) return cuda_fail(e, "fp32 launch");
-        record_launch(B * Hq, (Tq + 15) / 16, kernels);
-        return ok();
+    return dispatch(q, k, v, o, lse, s, dtype, env);
+}
+
+attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int Tq, int Tk, int D, int causal, float scale,
+                          attn_dtype dtype, cudaStream_t stream) {
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16 && dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    attn_status st = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, D, causal, scale);
+    if (st != ATTN_OK) return st;
+    LaunchEnv env;
+    st = device_env(stream, &env);
+    if (st != ATTN_OK) return st;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        DeviceState& d = g_dev[env.device];
+        if (d.h2d == nullptr) {
+            cudaError_t e = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking);
+            if (e != cudaSuccess) {
+                d.h2d = d.d2h = nullptr;
+                return cuda_fail(e, "creating the copy streams");
+            }
+        }
+        h2d = d.h2d;
+        d2h = d.d2h;
     }
-    if (Tq == 1) return run_decode(q, k, v, o, lse, s, 0, env);
-    return run_prefill(q, k, v, o, lse, s, env);
+    // Device copies of the five tensors in one stream-ordered allocation.
+    const size_t el = dtype == ATTN_F32 ? 4 : 2;
+    const size_t q_bytes = static_cast<size_t>(B) * Hq * Tq * D * el;
+    const size_t kv_bytes = static_cast<size_t>(B) * Hkv * Tk * D * el;
+    const size_t l_bytes = lse ? static_cast<size_t>(B) * Hq * Tq * sizeof(float) : 0;
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const size_t off_k = up(q_bytes), off_v = off_k + up(kv_bytes), off_o = off_v + up(kv_bytes);
+    const size_t off_l = off_o + up(q_bytes), total = off_l + up(l_bytes);
+    uint8_t* ws = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&ws), total, env.stream);
+    if (e != cudaSuccess || ws == nullptr) {
+        cudaGetLastError();
+        return fail(ATTN_ERR_NO_MEMORY, "device buffers of %zu bytes: %s", total,
+                    cudaGetErrorString(e));
+    }
+    // Units: (b, hkv) pairs.  A contiguous range of units is a contiguous byte
+    // range of every tensor and is itself a problem of shape [units, g, T, D]
+    // against [units, 1, T, D]: the chunks are copied in, computed and copied
+    // out on three streams, so that chunk c's compute overlaps chunk c+1's
+    // inputs and chunk c-1's outputs.
+    const int units = B * Hkv, g = Hq / Hkv;
+    const int chunks = units < kHostChunks ? units : kHostChunks;
+    const size_t uq = q_bytes / units, ukv = kv_bytes / units, ul = l_bytes / units;
+    cudaEvent_t ev[2 * kHostChunks + 2];
+    int n_ev = 0;
+    for (; n_ev < 2 * chunks + 2; ++n_ev) {
+        e = cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming);
+        if (e != cudaSuccess) break;
+    }
+    const char* what = "creating events";
+    int kernels = 0, grid = 0;
+    if (e == cudaSuccess) {
+        cudaEvent_t ev_start = ev[0], ev_end = ev[1];
+        cudaEvent_t* ev_in = ev + 2;
+        cudaEvent_t* ev_out = ev + 2 + chunks;
+        const uint8_t* qh = static_cast<const uint8_t*>(q);
+        const uint8_t* kh = static_cast<const uint8_t*>(k);
+        const uint8_t* vh = static_cast<const uint8_t*>(v);
+        uint8_t* oh = static_cast<uint8_t*>(o);
+        uint8_t* lh = reinterpret_cast<uint8_t*>(lse);
+        what = "ordering the copy streams";
+        e = cudaEventRecord(ev_start, env.stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h2d, ev_start, 0);
+        for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+            const size_t u0 = static_cast<size_t>(c) * units / chunks;
+            const size_t u1 = static_cast<size_t>(c + 1) * units / chunks;
+            what = "host-to-device copy";
+            e = cudaMemcpyAsync(ws + u0 * uq, qh + u0 * uq, (u1 - u0) * uq, cudaMemcpyHostToDevice, h2d);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(ws + off_k + u0 * ukv, kh + u0 * ukv, (u1 - u0) * ukv,
+                                    cudaMemcpyHostToDevice, h2d);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(ws + off_v + u0 * ukv, vh + u0 * ukv, (u1 - u0) * ukv,
+                                    cudaMemcpyHostToDevice, h2d);
+            if (e == cudaSuccess) e = cudaEventRecord(ev_in[c], h2d);
+        }
+        for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+            const size_t u0 = static_cast<size_t>(c) * units / chunks;
+            const size_t u1 = static_cast<size_t>(c + 1) * units / chunks;
+            what = "ordering the compute stream";
+            e = cudaStreamWaitEvent(env.stream, ev_in[c], 0);
+            if (e != cudaSuccess) break;
+            Shape s{static_cast<int>(u1 - u0), g, 1, Tq, Tk, D, causal ? 1 : 0, scale};
+            s.f16 = dtype == ATTN_F16 ? 1 : 0;
+            st = dispatch(ws + u0 * uq, ws + off_k + u0 * ukv, ws + off_v + u0 * ukv,
+                          ws + off_o + u0 * uq,
+                          lse ? reinterpret_cast<float*>(ws + off_l + u0 * ul) : nullptr, s, dtype,
+                          env);
+            if (st != ATTN_OK) break;
+            kernels += t_last_kernels;
+            grid = t_last_grid > grid ? t_last_grid : grid;
+            e = cudaEventRecord(ev_out[c], env.stream);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(d2h, ev_out[c], 0);
+            what = "device-to-host copy";
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(oh + u0 * uq, ws + off_o + u0 * uq, (u1 - u0) * uq,
+                                    cudaMemcpyDeviceToHost, d2h);
+            if (e == cudaSuccess && lse)
+                e = cudaMemcpyAsync(lh + u0 * ul, ws + off_l + u0 * ul, (u1 - u0) * ul,
+                                    cudaMemcpyDeviceToHost, d2h);
+        }
+        if (e == cudaSuccess && st == ATTN_OK) {
+            what = "joining the copy streams";
+            e = cudaEventRecord(ev_end, d2h);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(env.stream, ev_end, 0);
+        }
+    }
+    cudaError_t f = cudaFreeAsync(ws, env.stream);
+    for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+    if (st != ATTN_OK) return st;
+    if (e == cudaSuccess) e = f;
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    record_launch(grid, chunks, kernels);
+    return ok();
 }
 
 attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
