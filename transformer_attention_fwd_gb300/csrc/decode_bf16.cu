@@ -593,43 +593,6 @@ __device__ __forceinline__ int paged_block_id(const StreamParams& p, int b, int 
     return blk;
 }
 
-// Bulk copies of keys [kc, kc + n) of a paged unit into a ring stage, one
-// per run of rows inside one block; pages pg0 + r0 .. pg0 + r0 + cnt - 1 of
-// the chunk, whose block ids are ids[0 .. cnt-1] (cnt <= 8).
-template <int D>
-__device__ __forceinline__ void copy_paged_pages(uint8_t* stage, int half_bytes,
-                                                 const StreamParams& p, const Segment& sg, int kc,
-                                                 int n, int r0, int cnt, const int (&ids)[8],
-                                                 uint64_t* bar) {
-    const int P = p.pg.page;
-    const int64_t head_rows = static_cast<int64_t>(P) * D;  // one head of one block
-    const int64_t block_elems = 2 * static_cast<int64_t>(p.Hkv) * head_rows;
-    const int pg0 = kc / P;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (i >= cnt) break;
-        const int page = pg0 + r0 + i;
-        const int t = max(kc, page * P);
-        const int t1 = min(kc + n, page * P + P);
-        const uint16_t* kbase = p.pg.kv + static_cast<int64_t>(ids[i]) * block_elems +
-                                static_cast<int64_t>(sg.hkv) * head_rows +
-                                static_cast<int64_t>(t - page * P) * D;
-        const uint32_t bytes = static_cast<uint32_t>(t1 - t) * D * 2;
-        const int off = (t - kc) * D * 2;
-        bulk_load(stage + off, kbase, bytes, bar);
-        bulk_load(stage + half_bytes + off, kbase + static_cast<int64_t>(p.Hkv) * head_rows, bytes,
-                  bar);
-    }
-}
-
-// Block ids of pages first .. first + cnt - 1 of request b (cnt <= 8), as
-// independent loads.
-__device__ __forceinline__ void load_block_ids(const StreamParams& p, int b, int first, int cnt,
-                                               int (&ids)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ids[i] = (i < cnt) ? paged_block_id(p, b, first + i) : 0;
-}
-
 // Nine warps put three on one SM sub-partition, whose 16K registers cap a
 // thread at 168 (HC = 8 spills a little; splitting the heads would re-read K/V).
 // kPaged: keys come from the paged cache, per-request lengths, and cut units
@@ -673,42 +636,64 @@ decode_stream_kernel(const StreamParams p) {
     };
 
     if (warp == kStreamWarps && kPaged) {
-        // Producer (paged): lane 0 alone, like the dense producer (warp-wide
-        // operations would wait for its bulk copies to be taken by the copy
-        // engine).  The block ids of a chunk's first 8 pages are loaded as
-        // independent loads before the stage wait.
-        if (lane == 0) {
-            uint32_t it = 0;
-            long long v = v_begin;
-            Segment sg;
-            while (next(v, sg)) {
-                for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
-                    const int n = min(CK, sg.k1 - kc);
-                    const int s = it % kStreamStages;
-                    const int pg0 = kc / p.pg.page;
-                    const int np = (kc + n - 1) / p.pg.page - pg0 + 1;
-                    int ids[8];
-                    load_block_ids(p, sg.b, pg0, min(8, np), ids);
-                    if (it >= (uint32_t)kStreamStages &&
-                        !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY))
-                        goto drain_paged;
-                    uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
+        // Producer (paged): the lanes of the warp issue a chunk's copies
+        // together.  Lane 2i copies the K rows of the chunk's page i and lane
+        // 2i+1 its V rows; each lane loads and checks its own block id, so the
+        // ids, the address arithmetic and the copies of up to 8 pages take one
+        // pass instead of a serial chain in one lane.  Pages beyond the first
+        // 8 (blocks of fewer than 8 keys) repeat the pass.  (Loading the next
+        // chunk's ids while this chunk is issued measured slower: a lane's
+        // outstanding loads delay its copy issue.)  Every lane runs the
+        // same loop and waits on the stage barrier by itself: no warp-wide
+        // vote or shuffle, which would wait for the issued copies to be taken
+        // by the copy engine.
+        const int P = p.pg.page;
+        const int pi = lane >> 1;
+        const bool is_v = (lane & 1) != 0;
+        const int64_t head_rows = static_cast<int64_t>(P) * D;
+        const int64_t block_elems = 2 * static_cast<int64_t>(p.Hkv) * head_rows;
+        uint32_t it = 0;
+        long long v = v_begin;
+        Segment sg;
+        bool ok = true;
+        while (ok && next(v, sg)) {
+            const uint16_t* seg_base = p.pg.kv + static_cast<int64_t>(sg.hkv) * head_rows +
+                                       (is_v ? static_cast<int64_t>(p.Hkv) * head_rows : 0);
+            for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
+                const int n = min(CK, sg.k1 - kc);
+                const int s = it % kStreamStages;
+                const int pg0 = kc / P;
+                const int np = (kc + n - 1) / P - pg0 + 1;
+                int id = (lane < 16 && pi < np) ? paged_block_id(p, sg.b, pg0 + pi) : 0;
+                if (it >= (uint32_t)kStreamStages &&
+                    !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
+                if (lane == 0)
                     mbar_arrive_expect_tx(&bars->full[s], 2u * static_cast<uint32_t>(n) * D * 2);
-                    for (int r0 = 0; r0 < np; r0 += 8) {
-                        if (r0 > 0) load_block_ids(p, sg.b, pg0 + r0, min(8, np - r0), ids);
-                        copy_paged_pages<D>(stage, kHalf, p, sg, kc, n, r0, min(8, np - r0), ids,
-                                            &bars->full[s]);
+                for (int r0 = 0; r0 < np; r0 += 8) {
+                    if (r0 > 0) id = (lane < 16 && r0 + pi < np) ? paged_block_id(p, sg.b, pg0 + r0 + pi) : 0;
+                    const int page = pg0 + r0 + pi;
+                    if (lane < 16 && r0 + pi < np) {
+                        const int t = max(kc, page * P);
+                        const int t1 = min(kc + n, page * P + P);
+                        const uint16_t* src = seg_base + static_cast<int64_t>(id) * block_elems +
+                                              static_cast<int64_t>(t - page * P) * D;
+                        bulk_load(stage + (is_v ? kHalf : 0) + (t - kc) * D * 2, src,
+                                  static_cast<uint32_t>(t1 - t) * D * 2, &bars->full[s]);
                     }
                 }
             }
-            goto out_paged;
-        drain_paged:
+        }
+        if (!ok && lane == 0) {
+            // Let copies already in flight land before the CTA leaves.
             for (uint32_t i = (it > (uint32_t)kStreamStages ? it - kStreamStages : 0); i < it; ++i) {
                 const uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(&bars->full[i % kStreamStages], (i / kStreamStages) & 1))
                     if (global_timer_ns() - t0 > 200000000ull) break;
             }
-        out_paged:;
         }
     } else if (warp == kStreamWarps) {
         // Producer: bulk-copy every chunk of this CTA's slice into the ring.
