@@ -734,20 +734,25 @@ decode_stream_kernel(const StreamParams p) {
         while (next(v, sg)) {
             const int b = sg.b;
             const int hq0 = sg.hkv * p.group + sg.chunk * HC;
-            float qf[HC][8];
+            // Query and output columns as packed fp32 pairs: the dot products
+            // and the P.V updates run two columns per f32x2 instruction.
+            uint64_t qf2[HC][4];
 #pragma unroll
             for (int h = 0; h < HC; ++h) {
                 const uint16_t* qp = p.q + (static_cast<int64_t>(b) * p.Hq + hq0 + h) * D + sub * 8;
-                unpack8<kF16>(*reinterpret_cast<const uint4*>(qp), qf[h]);
+                float qf[8];
+                unpack8<kF16>(*reinterpret_cast<const uint4*>(qp), qf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) qf[h][e] *= p.scale_log2;
+                for (int e = 0; e < 4; ++e)
+                    qf2[h][e] = f2_pack(qf[2 * e] * p.scale_log2, qf[2 * e + 1] * p.scale_log2);
             }
-            float m[HC], acc[HC][8], lsum[NV];
+            float m[HC], lsum[NV];
+            uint64_t acc2[HC][4];
 #pragma unroll
             for (int h = 0; h < HC; ++h) {
                 m[h] = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = 0.0f;
+                for (int e = 0; e < 4; ++e) acc2[h][e] = 0ull;
             }
 #pragma unroll
             for (int r = 0; r < NV; ++r) lsum[r] = 0.0f;
@@ -778,12 +783,17 @@ decode_stream_kernel(const StreamParams p) {
                 for (int nn = 0; nn < kNK; ++nn) {
                     float kf[8];
                     unpack8<kF16>(kr[nn], kf);
+                    uint64_t kf2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) kf2[e] = f2_pack(kf[2 * e], kf[2 * e + 1]);
 #pragma unroll
                     for (int h = 0; h < HC; ++h) {
-                        float sacc = 0.0f;
+                        uint64_t s2 = f2_fma(qf2[h][0], kf2[0], 0ull);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) sacc = fmaf(qf[h][e], kf[e], sacc);
-                        part[nn * HC + h] = sacc;
+                        for (int e = 1; e < 4; ++e) s2 = f2_fma(qf2[h][e], kf2[e], s2);
+                        float s_lo, s_hi;
+                        f2_unpack(s2, s_lo, s_hi);
+                        part[nn * HC + h] = s_lo + s_hi;
                     }
                 }
                 group_reduce_scatter<NV0, LPK>(part, lane);
@@ -810,8 +820,9 @@ decode_stream_kernel(const StreamParams p) {
                         cm = warp_allmax(cm);
                         const float mnew = fmaxf(m[h], cm);
                         const float alpha = (m[h] == -INFINITY) ? 0.0f : ex2_approx(m[h] - mnew);
+                        const uint64_t alpha2 = f2_pack(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[h][e] *= alpha;
+                        for (int e = 0; e < 4; ++e) acc2[h][e] = f2_fma(acc2[h][e], alpha2, 0ull);
 #pragma unroll
                         for (int r = 0; r < NV; ++r) lsum[r] = (hown[r] == h) ? lsum[r] * alpha : lsum[r];
                         m[h] = mnew;
@@ -838,11 +849,15 @@ decode_stream_kernel(const StreamParams p) {
                 for (int nn = 0; nn < kNK; ++nn) {
                     float vf[8];
                     unpack8<kF16>(vr[nn], vf);
+                    uint64_t vf2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) vf2[e] = f2_pack(vf[2 * e], vf[2 * e + 1]);
 #pragma unroll
                     for (int h = 0; h < HC; ++h) {
                         const float pw = pall[nn * HC + h];
+                        const uint64_t pw2 = f2_pack(pw, pw);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
+                        for (int e = 0; e < 4; ++e) acc2[h][e] = f2_fma(pw2, vf2[e], acc2[h][e]);
                     }
                 }
                 // Every value read from the stage has been used: release it.
@@ -851,6 +866,11 @@ decode_stream_kernel(const StreamParams p) {
             }
 
             // Segment end: merge lane groups, then warps (block-merge rule).
+            float acc[HC][8];
+#pragma unroll
+            for (int h = 0; h < HC; ++h)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_unpack(acc2[h][e], acc[h][2 * e], acc[h][2 * e + 1]);
 #pragma unroll
             for (int mask = LPK; mask < 32; mask <<= 1) {
 #pragma unroll
