@@ -766,17 +766,13 @@ decode_stream_kernel(const StreamParams p) {
                 const uint8_t* ks = smem + L::kRingOff + s * kStageBytes;
                 const uint8_t* vs = ks + kHalf;
                 const int kb = warp * KW;
-                uint4 kr[kNK], vr[kNK];
+                // K rows now; V rows after the scores (fewer registers live).
+                uint4 kr[kNK];
 #pragma unroll
                 for (int nn = 0; nn < kNK; ++nn) {
                     const int key = kb + nn * KPL + grp;
-                    if (key < n) {
-                        kr[nn] = *reinterpret_cast<const uint4*>(ks + key * D * 2 + sub * 16);
-                        vr[nn] = *reinterpret_cast<const uint4*>(vs + key * D * 2 + sub * 16);
-                    } else {
-                        kr[nn] = make_uint4(0, 0, 0, 0);
-                        vr[nn] = make_uint4(0, 0, 0, 0);
-                    }
+                    kr[nn] = key < n ? *reinterpret_cast<const uint4*>(ks + key * D * 2 + sub * 16)
+                                     : make_uint4(0, 0, 0, 0);
                 }
                 float part[NV0];
 #pragma unroll
@@ -838,23 +834,24 @@ decode_stream_kernel(const StreamParams p) {
                     if (own_canonical<NV0, LPK>(sub)) s_p[warp][grp][own_index<NV0, LPK>(sub, r)] = pr;
                 }
                 __syncwarp();
-                float pall[NV0];
-#pragma unroll
-                for (int i = 0; i < NV0; i += 4) {
-                    const float4 t = *reinterpret_cast<const float4*>(&s_p[warp][grp][i]);
-                    pall[i] = t.x; pall[i + 1] = t.y; pall[i + 2] = t.z; pall[i + 3] = t.w;
-                }
-                __syncwarp();
 #pragma unroll
                 for (int nn = 0; nn < kNK; ++nn) {
+                    const int key = kb + nn * KPL + grp;
+                    const uint4 vr = key < n ? *reinterpret_cast<const uint4*>(vs + key * D * 2 + sub * 16)
+                                             : make_uint4(0, 0, 0, 0);
+                    // This key's weights for the HC heads (one key at a time: fewer
+                    // registers live than all NV0 at once).
+                    float pk[HC];
+#pragma unroll
+                    for (int h = 0; h < HC; ++h) pk[h] = s_p[warp][grp][nn * HC + h];
                     float vf[8];
-                    unpack8<kF16>(vr[nn], vf);
+                    unpack8<kF16>(vr, vf);
                     uint64_t vf2[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) vf2[e] = f2_pack(vf[2 * e], vf[2 * e + 1]);
 #pragma unroll
                     for (int h = 0; h < HC; ++h) {
-                        const float pw = pall[nn * HC + h];
+                        const float pw = pk[h];
                         const uint64_t pw2 = f2_pack(pw, pw);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc2[h][e] = f2_fma(pw2, vf2[e], acc2[h][e]);
