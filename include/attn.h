@@ -86,7 +86,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o,
  * those of attn_fwd, with host pointers (16-byte aligned; page-locked memory,
  * cudaMallocHost or cudaHostRegister, lets the copies overlap the compute,
  * pageable memory works but serialises them).
- * The (b, hkv) pairs are cut into up to four contiguous chunks; each chunk is
+ * The (b, hkv) pairs are cut into up to five contiguous chunks (the first and
+ * last smaller than the others); each chunk is
  * copied in on one copy stream, computed on `stream` (as attn_fwd with B =
  * its pairs, Hq = Hq / Hkv, Hkv = 1) and copied out on another, so the copies
  * of one chunk overlap the compute of its neighbours.  Device buffers for the
