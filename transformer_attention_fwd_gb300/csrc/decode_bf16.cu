@@ -22,6 +22,17 @@
 //    any common reference value gives the same normalised result).
 //  * Each split writes its normalised partial output and its log-sum-exp;
 //    the combine kernel merges the splits with the block-merge rule of §12.3.
+//
+// The default (automatic) mode is the stream-K kernel further down: the keys
+// of all (b, hkv, head chunk) units are laid end to end and cut into one
+// equal slice per SM; a producer warp bulk-copies each chunk of K and V rows
+// into a shared-memory ring and eight consumer warps apply the arithmetic
+// above (with the query columns and output accumulators as packed fp32
+// pairs, two columns per f32x2 instruction).  Units cut by a slice boundary
+// leave fragments that a combine kernel merges.  The same kernel reads a
+// paged cache (kPaged: per-request lengths, block-table indirection, the
+// producer warp's lanes issuing a chunk's per-block copies together) and
+// fp16 instead of bf16 elements (kF16).
 #include <cuda_runtime.h>
 #include <cmath>
 #include <cstdint>

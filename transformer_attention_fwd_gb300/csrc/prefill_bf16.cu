@@ -1,5 +1,5 @@
-// prefill_bf16.cu -- bf16 attention forward on the 5th-generation tensor
-// cores (tcgen05), fp32 accumulation in tensor memory.
+// prefill_bf16.cu -- bf16 (or fp16) attention forward on the 5th-generation
+// tensor cores (tcgen05), fp32 accumulation in tensor memory.
 //
 // The method is the tiled attention with online softmax of
 // "3.3 Self-Attention机制深入理解" §12.2/§12.3: for every tile of query rows
@@ -27,8 +27,13 @@
 // tile's products; every tile is spread over two warps per SM sub-partition,
 // which halves the latency of its softmax against one warp per row quarter.
 // The softmax computes a row maximum only on a row's first tile and on the
-// rare tile whose weights outgrow 2^64; every other tile is weighted against
-// the running reference directly.
+// rare tile whose weights outgrow 2^64 (2^17 for fp16); every other tile is
+// weighted against the running reference directly.
+//
+// Template arguments: head dim D, kPacked (sequences packed along the token
+// axis of (T, H, D) tensors, one record per work item written by the
+// scheduling kernels of varlen_sched.cu), kF16 (fp16 instead of bf16 I/O).
+// A runtime window (> 0) limits each row to its most recent keys.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <climits>
