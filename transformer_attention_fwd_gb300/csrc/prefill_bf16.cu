@@ -71,15 +71,23 @@ struct Cfg {
     static constexpr int kQStages = (D == 128) ? 1 : 2;    // Q buffers (2 query tiles each)
     static constexpr int kKStages = (D == 128) ? 3 : 4;
     static constexpr int kVStages = (D == 128) ? 2 : 4;
+    // At D = 64 the P.V product also sums the rounded weights: its B operand
+    // gets 16 more columns from a constant box of ones, so O carries
+    // sum_k bf16(P[r, k]) in columns D .. D+15 and the softmax does not add
+    // them up (tensor memory has room: 2 x (64 + 16) + 256 columns).
+    static constexpr int kLrCols = (D == 64) ? 16 : 0;
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQStages * NQT * kTileBytes;
     static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-    static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+    static constexpr int kOnesOff = kVOff + kVStages * kTileBytes;  // 128 x 64 ones (kLrCols)
+    static constexpr int kBarOff = kOnesOff + (kLrCols ? kBoxBytes : 0);
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;  // + 1024-byte alignment slack
     // Tensor-memory columns of the S/P and O accumulators of query tile t.
     __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
-    __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+    __device__ static constexpr uint32_t col_o(int t) {
+        return 256u + static_cast<uint32_t>(D + kLrCols) * t;
+    }
 };
 
 // Register split (setmaxnreg): the CTA launches with 168 registers per thread
@@ -270,10 +278,12 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t qd, uint64_t 
 // O[tmem cols] (+)= P . V_tile : M = 128, N = D, K = 128 keys in steps of 16.
 // P is read from tensor memory (8 columns per 16 keys); V is MN-major, K step
 // kk starts 16 key rows (2 KB) further.  vd: descriptor of the V tile.
-template <int D, bool kF16 = false>
+// kExtra > 0: N = D + kExtra, the extra columns read from the 64-column atom
+// at vd's leading-dimension offset (the box of ones).
+template <int D, bool kF16 = false, int kExtra = 0>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vd,
                                          bool accumulate, uint32_t leader) {
-    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D, false, true, kF16);
+    constexpr uint32_t idesc = mma_idesc_bf16_f32(BM, D + kExtra, false, true, kF16);
     uint32_t a[BN / 16];
     uint64_t b[BN / 16];
 #pragma unroll
@@ -399,6 +409,18 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
     const uint64_t q_desc0 = smem_desc_sw128(smem_u32(smem + C::kQOff), 16, 1024);
     const uint64_t k_desc0 = smem_desc_sw128(smem_u32(smem + C::kKOff), 16, 1024);
     const uint64_t v_desc0 = smem_desc_sw128(smem_u32(smem + C::kVOff), kBoxBytes, 1024);
+    // With the rounded-weight columns (D = 64) a V stage's descriptor also
+    // locates the box of ones: it follows the V ring, one leading-dimension
+    // offset past the stage, so stage s has start +s tiles and offset -s
+    // tiles (both fields stay in range: no carry between them).
+    const uint64_t v_desc_lr0 =
+        smem_desc_sw128(smem_u32(smem + C::kVOff), C::kOnesOff - C::kVOff, 1024);
+    auto v_desc_of = [&](uint32_t stage) -> uint64_t {
+        if constexpr (C::kLrCols > 0)
+            return v_desc_lr0 + stage * kTile16 - (static_cast<uint64_t>(stage * kTile16) << 16);
+        else
+            return desc_advance(v_desc0, stage * kTile16);
+    };
     // Rolling ring positions: stage and phase parity of the next K and V tile
     // and of the V tile of the previous key tile (read by PV1 one step late).
     uint32_t ks = 0, kph = 0, vs = 0, vph = 0, pvs = 0, pvph = 0;
@@ -421,7 +443,7 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
         const uint64_t q_desc = desc_advance(q_desc0, qs * NQT * kTile16);
         for (int j = lo0; j <= nkv; ++j) {
             const uint64_t k_desc = desc_advance(k_desc0, ks * kTile16);
-            const uint64_t v_desc = desc_advance(v_desc0, vs * kTile16);
+            const uint64_t v_desc = v_desc_of(vs);
             if (j < nkv) {
                 if (!warp_wait(&bars->k_full[ks], kph, g, SITE_K_FULL)) goto drain;
                 tc_fence_after_sync();
@@ -438,8 +460,8 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                     !warp_wait(&bars->o_empty[1], (o_cnt[1] - 1) & 1, g, SITE_O_EMPTY))
                     goto drain;
                 tc_fence_after_sync();
-                issue_pv<D, kF16>(tmem + C::col_o(1), tmem + C::col_s(1),
-                            desc_advance(v_desc0, pvs * kTile16), j - 1 > lo1, leader);
+                issue_pv<D, kF16, C::kLrCols>(tmem + C::col_o(1), tmem + C::col_s(1),
+                                              v_desc_of(pvs), j - 1 > lo1, leader);
                 if (j - 1 == n1 - 1) {
                     mma_commit(&bars->o_full[1], leader);
                     ++o_cnt[1];
@@ -462,8 +484,8 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Prefi
                         !warp_wait(&bars->o_empty[0], (o_cnt[0] - 1) & 1, g, SITE_O_EMPTY))
                         goto drain;
                     tc_fence_after_sync();
-                    issue_pv<D, kF16>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc, j > lo0,
-                                      leader);
+                    issue_pv<D, kF16, C::kLrCols>(tmem + C::col_o(0), tmem + C::col_s(0), v_desc,
+                                                  j > lo0, leader);
                     if (j == n0 - 1) {
                         mma_commit(&bars->o_full[0], leader);
                         ++o_cnt[0];
@@ -493,7 +515,9 @@ drain:
 // in .16x128b order (p[2n] row a, p[2n+1] row b, both P column 4n + i%4, i.e.
 // keys 8n + 2(i%4) and +1); se/sr receive this thread's exact and
 // bf16-rounded partial row sums.
-template <bool kPoly, bool kF16>
+// kSumRounded: also sum the rounded weights (sr); false when the P.V
+// product sums them in its extra columns.
+template <bool kPoly, bool kF16, bool kSumRounded = true>
 __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_log2,
                                           float neg_ma, float neg_mb, uint32_t (&p)[32],
                                           float (&se)[2], float (&sr)[2]) {
@@ -520,7 +544,7 @@ __device__ __forceinline__ void tile_exp2(const uint32_t (&s)[64], float scale_l
             }
             const uint32_t pk = Elem16<kF16>::pack(e0, e1);
             acc_e[r][n & 1] = f2_add(acc_e[r][n & 1], f2_pack(e0, e1));
-            Elem16<kF16>::add2(pk, acc_r[r][0], acc_r[r][1]);
+            if constexpr (kSumRounded) Elem16<kF16>::add2(pk, acc_r[r][0], acc_r[r][1]);
             p[2 * n + r] = pk;
         }
     }
@@ -572,6 +596,8 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
                                              bool mask_r, bool mask_l, int key0, int lim_a,
                                              int lim_b, int lft_a, int lft_b, bool first,
                                              float scale_log2) {
+    constexpr int kLr = Cfg<D>::kLrCols;
+    constexpr bool kSumR = kLr == 0;
     uint32_t s[64];
     tmem_ld_16x256b_x16(s_addr, s);
     tmem_wait_ld64(s);
@@ -589,9 +615,9 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
     bool exact = first;
     if (!first) {
         if (masked)
-            tile_exp2<false, kF16>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+            tile_exp2<false, kF16, kSumR>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
         else
-            tile_exp2<true, kF16>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
+            tile_exp2<true, kF16, kSumR>(s, scale_log2, -st.m[0], -st.m[1], pk, se, sr);
         exact = !(se[0] <= Elem16<kF16>::kMaxPartial) || !(se[1] <= Elem16<kF16>::kMaxPartial);
     }
     if (__any_sync(0xffffffffu, exact)) {
@@ -634,13 +660,22 @@ __device__ __forceinline__ void softmax_tile(RowState& st, uint32_t s_addr, uint
                     ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha[(i >> 1) & 1]);
                 tmem_st_16x256b_x8(o_addr + 64 * c, ov);
             }
+            if constexpr (kLr > 0) {  // the rounded-weight columns move with O
+                uint32_t lv[8];
+                tmem_ld_16x256b_x2(o_addr + D, lv);
+                tmem_wait_ld8(lv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    lv[i] = __float_as_uint(__uint_as_float(lv[i]) * alpha[(i >> 1) & 1]);
+                tmem_st_16x256b_x2(o_addr + D, lv);
+            }
         }
         const float nma = (st.m[0] == -INFINITY) ? 0.0f : -st.m[0];
         const float nmb = (st.m[1] == -INFINITY) ? 0.0f : -st.m[1];
         if (masked)
-            tile_exp2<false, kF16>(s, scale_log2, nma, nmb, pk, se, sr);
+            tile_exp2<false, kF16, kSumR>(s, scale_log2, nma, nmb, pk, se, sr);
         else
-            tile_exp2<true, kF16>(s, scale_log2, nma, nmb, pk, se, sr);
+            tile_exp2<true, kF16, kSumR>(s, scale_log2, nma, nmb, pk, se, sr);
     }
     // P overwrites the first 64 columns of the tile (keys 2j, 2j+1 in column j).
     tmem_st_16x128b_x16(s_addr, pk);
@@ -731,6 +766,14 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                 lr[r] = st[t].lr[r] + __shfl_xor_sync(0xffffffffu, st[t].lr[r], 1);
                 lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], 2);
             }
+            if constexpr (C::kLrCols > 0) {
+                // The P.V product summed the rounded weights in columns D..D+15.
+                uint32_t lv[8];
+                tmem_ld_16x256b_x2(lanes + C::col_o(t) + D, lv);
+                tmem_wait_ld8(lv);
+                lr[0] = __uint_as_float(lv[0]);
+                lr[1] = __uint_as_float(lv[2]);
+            }
             const float inv[2] = {1.0f / lr[0], 1.0f / lr[1]};
             const int r0 = it.qb * kItemRows + t * BM;
             const int row[2] = {r0 + ra, r0 + ra + 8};
@@ -808,6 +851,14 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
+    }
+    if constexpr (C::kLrCols > 0) {
+        // The box of ones (every column, so any swizzle reads 1.0), written
+        // through the generic proxy and fenced for the tensor core's reads.
+        const uint32_t one2 = kF16 ? 0x3C003C00u : 0x3F803F80u;
+        uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::kOnesOff);
+        for (int i = threadIdx.x; i < kBoxBytes / 4; i += kThreads) ones[i] = one2;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     tc_fence_before_sync();
     __syncthreads();
