@@ -1,14 +1,9 @@
 """Shared helpers for the GPU parity tests (marked ``gpu``)."""
 from __future__ import annotations
 
-import math
-
 import numpy as np
 import pytest
 import torch
-
-import oracle
-from transformer_attention_fwd_gb300.inputs import make_qkv
 
 # Tolerances (max abs error against the float64 oracle on the same inputs).
 TOL_O_F32 = 1e-5      # fp32 I/O

@@ -1,7 +1,5 @@
 """Split-KV decode parity against the float64 oracle."""
-import numpy as np
 import pytest
-import torch
 
 import oracle
 from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, compare, to_dev

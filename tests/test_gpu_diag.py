@@ -1,6 +1,5 @@
 """Self-tests of the hardware building blocks (tensor-core tile products,
 bounded pipeline waits), run before the attention parity tests."""
-import numpy as np
 import pytest
 import torch
 

@@ -1,6 +1,5 @@
 """bf16 tensor-core prefill parity against the float64 oracle run on the same
 bf16-rounded inputs (max abs error 1e-2 on O, 1e-4 on lse)."""
-import numpy as np
 import pytest
 import torch
 
