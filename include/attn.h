@@ -149,10 +149,17 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
  * loading libattn.so holds until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
- * Size limit: the partials take B*Hq*splits*(D+1)*4 bytes and must fit in the
- * 8 MiB.  With num_splits = 0 the automatic split count is lowered until they
- * fit (one split needs no workspace at all); an explicit num_splits that does
- * not fit returns ATTN_ERR_UNSUPPORTED with the sizes in attn_last_error().
+ * Automatic mode (num_splits = 0) runs the same stream-K kernels as
+ * attn_fwd_decode whenever their fragment workspace fits in the 8 MiB:
+ * B*Hq*nseg*(D+1)*4 bytes (plus 256), where nseg = ceil(Tk / slice) + 1 and
+ * slice = ceil(B*Hkv*(Hq/Hkv/hc)*Tk / SMs) keys, hc being the heads one CTA
+ * serves (8, 4, 2 or 1, the largest that divides Hq/Hkv).  That holds for
+ * every shape with B*Hq <= 8128 query rows at D = 128 (16131 at D = 64).
+ * Above that the call uses the split kernel instead, with the automatic
+ * split count lowered until its partials, B*Hq*splits*(D+1)*4 bytes, fit (one
+ * split needs no workspace at all).  An explicit num_splits uses the split
+ * kernel; if its partials do not fit the call returns ATTN_ERR_UNSUPPORTED
+ * with the sizes in attn_last_error().
  *
  * Sharing: every call uses the same array and overwrites the part it reads
  * before reading it, so nothing has to start at zero; but calls whose kernels

@@ -69,9 +69,46 @@ def test_noalloc_rejects_partials_beyond_the_static_workspace():
     st, _, _ = _call(fn, q, k, v, splits)
     assert st == a.ATTN_ERR_UNSUPPORTED
     assert "static workspace" in a.last_error()
-    st, o, lse = _call(fn, q, k, v, 0)  # automatic count is capped to fit
+    st, o, lse = _call(fn, q, k, v, 0)  # automatic mode: the stream-K fragments fit
     assert st == a.ATTN_OK, a.last_error()
     o_ref, lse_ref = a.attn_fwd_decode(q, k, v)
     check_status(a)
     assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
     assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16
+
+
+def _stream_fits(B, Hq, Hkv, Tk, D, num_sms):
+    """Whether the stream-K fragments fit in the static workspace (the sizing
+    the header states for automatic mode)."""
+    group = Hq // Hkv
+    hc = next(h for h in (8, 4, 2, 1) if group % h == 0)
+    total = B * Hkv * (group // hc) * Tk
+    per = -(-total // num_sms)
+    nseg = -(-Tk // per) + 1
+    return B * Hq * nseg * (D + 1) * 4 + 256 <= SCRATCH_BYTES
+
+
+@pytest.mark.parametrize("B,expect_stream", [(254, True), (255, False)])
+def test_noalloc_automatic_mode_uses_stream_k_while_it_fits(B, expect_stream):
+    a, fn = _noalloc()
+    Hq, Hkv, Tk, D = 32, 8, 256, 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _stream_fits(B, Hq, Hkv, Tk, D, sms) == expect_stream
+    q, k, v = to_dev(*make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=40 + B))
+    st, o, lse = _call(fn, q, k, v, 0)
+    assert st == a.ATTN_OK, a.last_error()
+    grid, items, _ = a.last_launch_info()
+    torch.cuda.synchronize()
+    check_status(a)
+    o_ref, lse_ref = a.attn_fwd_decode(q, k, v)
+    grid_ref, _, _ = a.last_launch_info()
+    check_status(a)
+    if expect_stream:
+        # The same kernels on the same slices as attn_fwd_decode: equal bits.
+        assert grid == grid_ref <= sms and items == 0
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    else:
+        # The split kernel: one CTA row per (b, hkv), tolerance of the split path.
+        assert grid == B * Hkv and items >= 1
+        assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
+        assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16

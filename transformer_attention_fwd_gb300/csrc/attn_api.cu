@@ -789,6 +789,23 @@ extern "C" attn_status attn_fwd_decode_noalloc(const void* q, const void* k, con
     st = device_env(stream, &env);
     if (st != ATTN_OK) return st;
     const Shape s{B, Hq, Hkv, 1, Tk, D, 0, scale};
+    if (num_splits == 0 && decode_stream_workspace_bytes(s, env.num_sms) <= kNoAllocScratchBytes) {
+        // Automatic mode: the stream-K kernels of attn_fwd_decode, their
+        // fragments in the static array.
+        void* ws = nullptr;
+        st = noalloc_scratch(env.device, &ws);
+        if (st != ATTN_OK) return st;
+        int grid = 0, kernels = 0;
+        cudaError_t e = launch_decode_stream_bf16(
+            static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+            static_cast<const uint16_t*>(v), static_cast<uint16_t*>(o), lse,
+            static_cast<float*>(ws), s, env, &grid, &kernels);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+        record_launch(grid, 0, kernels);
+        return ok();
+    }
+    // Explicit split counts, and automatic mode when the stream-K fragments
+    // would not fit: the split kernel.
     int splits = nonempty_splits(num_splits > 0 ? num_splits : decode_choose_splits(s, env.num_sms), Tk);
     if (num_splits == 0)  // automatic count: lower it until the partials fit
         while (splits > 1 && noalloc_bytes(s, splits) > kNoAllocScratchBytes)
