@@ -121,7 +121,9 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v,
  * block-merge rule of "Self-Attention机制深入理解" §12.3.
  * num_splits: 0 = automatic: all keys of all (b, hkv) are laid end to end
  * and cut into one equal slice per SM, each slice streamed by one persistent
- * CTA (a (b, hkv) cut by a slice boundary is merged the same way).
+ * CTA (a (b, hkv) cut by a slice boundary is merged the same way); for MHA
+ * (Hq == Hkv) instead the split ranges below, their count chosen to fill the
+ * last wave of CTAs (measured faster there).
  * 1..256 = that many equal ranges per (b, hkv) (clamped to the number of
  * keys).  The result does not depend on the split choice beyond float32
  * rounding.  Partial results live in a workspace the library allocates and
@@ -149,8 +151,9 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
  * loading libattn.so holds until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
- * Automatic mode (num_splits = 0) runs the same stream-K kernels as
- * attn_fwd_decode whenever their fragment workspace fits in the 8 MiB:
+ * Automatic mode (num_splits = 0) runs the kernels attn_fwd_decode picks.
+ * For MHA (Hq == Hkv) that is the split kernel (next paragraph); otherwise
+ * the stream-K kernels, whenever their fragment workspace fits in the 8 MiB:
  * B*Hq*nseg*(D+1)*4 bytes (plus 256), where nseg = ceil(Tk / slice) + 1 and
  * slice = ceil(B*Hkv*(Hq/Hkv/hc)*Tk / SMs) keys, hc being the heads one CTA
  * serves (8, 4, 2 or 1, the largest that divides Hq/Hkv).  That holds for

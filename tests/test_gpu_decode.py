@@ -45,6 +45,7 @@ def test_decode_equals_prefill_kernel_at_tq1():
     (1, 1, 1, 1, 64, 0), (3, 4, 4, 7, 64, 0), (2, 32, 1, 1000, 128, 0),  # MHA tiny, MQA
     (2, 16, 2, 4097, 128, 0), (1, 8, 8, 513, 64, 5), (2, 12, 4, 129, 128, 1),
     (1, 6, 2, 2000, 64, 7),
+    (2, 64, 8, 1500, 64, 0), (3, 64, 8, 777, 128, 0),  # eight heads per KV head: two warp groups
 ])
 def test_decode_shapes(B, Hq, Hkv, Tk, D, splits):
     a = attn()

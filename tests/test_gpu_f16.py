@@ -31,7 +31,7 @@ def test_f16_prefill_matches_oracle(B, Hq, Hkv, Tq, Tk, D, causal):
     compare(o, lse, o_ref, lse_ref, TOL_O_F16, TOL_LSE_F16, f"f16 prefill {B,Hq,Hkv,Tq,Tk,D}")
 
 
-@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (16, 16, 64), (32, 1, 128)])
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (16, 16, 64), (32, 1, 128), (64, 8, 64)])
 def test_f16_decode_matches_oracle(Hq, Hkv, D):
     a = attn()
     q, k, v = make_qkv(4, Hq, Hkv, 1, 1500, D, "f16", seed=102)

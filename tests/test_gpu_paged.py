@@ -38,6 +38,7 @@ def _check(a, q, kv, bt, sl, what):
     (5, 32, 8, 128, 16, [4096, 1, 2048, 15, 16]),
     (3, 4, 2, 64, 1, [3, 40, 7]),                 # one token per block
     (2, 8, 2, 128, 256, [700, 256]),              # large blocks
+    (2, 16, 2, 64, 16, [100, 2000]),              # eight heads per KV head, D=64
 ])
 def test_paged_matches_oracle(B, Hq, Hkv, D, page, lens):
     a = attn()
