@@ -223,6 +223,23 @@ def cpu_oracle_rate(w, target_s, seed=0):
 # ---------------------------------------------------------------------------
 # GPU measurement
 # ---------------------------------------------------------------------------
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's x (x itself without a process group): the
+    job's time is its slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_per_step):
+    """Units per second of the whole job: every rank processes units_per_rank
+    per step, and a step takes the slowest rank's time."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
+
+
 def time_steps(fn, steps, warmup, flush=None):
     """Warm up, then time `steps` calls with CUDA events on the current stream,
     flushing L2 (outside the event pairs) before each call when asked."""
@@ -296,13 +313,9 @@ def run_ours(args, rank, world):
     st = attn.device_status()
     assert st == attn.ATTN_OK, attn.last_error()
 
-    total_ms = sum(times)
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times), dist, "cuda")
     ms_per_step = total_ms / args.steps
-    value = w.flops * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(w.flops, world, ms_per_step) / 1e12
     kernel_tflops = w.flops / (ms_per_step * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     traffic = load_traffic("prefill_llama3_t8192_causal", PREFILL_SOURCES)
