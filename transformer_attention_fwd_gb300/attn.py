@@ -99,6 +99,34 @@ def last_launch_info():
     return g.value, i.value, k.value
 
 
+def _check_buffer(name, t, shape, dtype, device):
+    """A caller-supplied output buffer must hold exactly what the call writes:
+    the kernels write through its pointer and know nothing of its size."""
+    if t is None:
+        return
+    if t.device != torch.device(device):
+        raise ValueError(f"{name} must be on {device} (got {t.device})")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != math.prod(shape):
+        raise ValueError(f"{name} must hold {tuple(shape)} = {math.prod(shape)} elements "
+                         f"(got {tuple(t.shape)})")
+
+
+def _same_device(**tensors):
+    """Every tensor on one CUDA device, the current one (the library launches
+    on the current device)."""
+    devs = {t.device for t in tensors.values()}
+    if len(devs) != 1:
+        raise ValueError(f"{', '.join(tensors)} must be on one device (got {sorted(map(str, devs))})")
+    dev = devs.pop()
+    if dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {dev} but the current device is "
+                         f"cuda:{torch.cuda.current_device()}; call under torch.cuda.device({dev})")
+
+
 def _shapes(q, k, v):
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
@@ -107,6 +135,7 @@ def _shapes(q, k, v):
             raise ValueError(f"{name} must be contiguous [B, H, T, D]")
         if t.dim() != 4:
             raise ValueError(f"{name} must be 4-D [B, H, T, D]")
+    _same_device(q=q, k=k, v=v)
     if not (q.dtype == k.dtype == v.dtype):
         raise ValueError("q, k, v must share a dtype")
     B, Hq, Tq, D = q.shape
@@ -118,6 +147,8 @@ def _shapes(q, k, v):
 
 def _outputs(q, out, lse, want_lse):
     B, Hq, Tq, D = q.shape
+    _check_buffer("out", out, q.shape, q.dtype, q.device)
+    _check_buffer("lse", lse, (B, Hq, Tq), torch.float32, q.device)
     o = torch.empty_like(q) if out is None else out
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
@@ -170,6 +201,8 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out
     if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D:
         raise ValueError("k and v must be [B, Hkv, Tk, D] with q's B and D")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_buffer("out", out, q.shape, q.dtype, "cpu")
+    _check_buffer("lse", lse, (B, Hq, Tq), torch.float32, "cpu")
     pin = q.is_pinned()
     o = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if out is None else out
     if lse is None and want_lse:
@@ -248,9 +281,12 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool, window: i
     if (cu_seqlens_q.dim() != 1 or cu_seqlens_q.shape != cu_seqlens_k.shape
             or cu_seqlens_q.shape[0] < 2):
         raise ValueError("cu_seqlens_q and cu_seqlens_k must be [B + 1]")
+    _same_device(q=q, k=k, v=v, cu_seqlens_q=cu_seqlens_q, cu_seqlens_k=cu_seqlens_k)
     total_q, Hq, D = q.shape
     total_k, Hkv, _ = k.shape
     B = cu_seqlens_q.shape[0] - 1
+    _check_buffer("out", out, q.shape, q.dtype, q.device)
+    _check_buffer("lse", lse, (Hq, total_q), torch.float32, q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None and want_lse:
@@ -287,6 +323,9 @@ def attn_fwd_decode_paged(q, kv_cache, block_table, seq_lens, scale: float | Non
     nblk, _, Hkv, page, Dk = kv_cache.shape
     if Dk != D or block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
         raise ValueError("block_table must be [B, max_pages] and seq_lens [B], with q's B and D")
+    _same_device(q=q, kv_cache=kv_cache, block_table=block_table, seq_lens=seq_lens)
+    _check_buffer("out", out, q.shape, q.dtype, q.device)
+    _check_buffer("lse", lse, (B, Hq), torch.float32, q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None and want_lse:
