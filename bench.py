@@ -493,6 +493,12 @@ def run_secondary(args, attn, peaks, flush):
     }
     del q, k, v, cq, ck, o, lse
     assert attn.device_status() == attn.ATTN_OK, attn.last_error()
+    # Prefill time against T (L2 flushed before each call).
+    out["t_sweep"] = {
+        "note": "bf16 prefill, L2 flushed before every call; growth = t(T) / t(T/2), "
+                "which tends to 4 once the T^2 work dominates the fixed per-call cost",
+        "steps_per_point": 20,
+        "points": sweep_points(attn, 20, 3, flush)}
     return out
 
 
@@ -587,18 +593,14 @@ SWEEP_SHAPES = [
 ]
 
 
-def run_sweep(args):
-    """Prefill time against sequence length: T = 64, 128, .., doubling. The
-    growth column is t(T) / t(T/2), which tends to 4 once the T^2 work
-    dominates the launch and pipeline-fill latency."""
+def sweep_points(attn, steps, warmup, flush):
+    """Prefill time against sequence length, T = 64, 128, .., doubling, for
+    each SWEEP_SHAPES entry ("第 11 章 · Attention 入门" §11 exercises: the
+    T sweep).  The growth column is t(T) / t(T/2), which tends to 4 once the
+    T^2 work dominates the launch and pipeline-fill latency."""
     import torch
-    from transformer_attention_fwd_gb300 import build as b
-    b.build()
-    from transformer_attention_fwd_gb300 import attn
     from transformer_attention_fwd_gb300.inputs import make_qkv
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    flush = lambda: flush_buf.fill_(1)  # noqa: E731
-    steps = max(5, min(args.steps, 200))
+    points = []
     for name, B, Hq, Hkv, D, causal, tmax in SWEEP_SHAPES:
         prev = None
         T = 64
@@ -606,18 +608,30 @@ def run_sweep(args):
             q, k, v = (x.cuda() for x in make_qkv(B, Hq, Hkv, T, T, D, "bf16", 0))
             o = torch.empty_like(q)
             fn = lambda: attn.attn_fwd(q, k, v, causal=causal, out=o, want_lse=False)  # noqa: E731
-            times = time_steps(fn, steps, max(3, args.warmup), flush)
+            times = time_steps(fn, steps, warmup, flush)
             ms = sum(times) / steps
             flops = 4.0 * B * Hq * T * T * D * (0.5 if causal else 1.0)
-            print(json.dumps({"sweep": name, "T": T, "ms_per_step": round(ms, 5),
-                              "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
-                              "growth": None if prev is None else round(ms / prev, 3)}),
-                  flush=True)
+            points.append({"sweep": name, "T": T, "ms_per_step": round(ms, 5),
+                           "tflops": round(flops / (ms * 1e-3) / 1e12, 3),
+                           "growth": None if prev is None else round(ms / prev, 3)})
             prev = ms
             T *= 2
             del q, k, v, o
     if attn.device_status() != attn.ATTN_OK:
         raise RuntimeError(attn.last_error())
+    return points
+
+
+def run_sweep(args):
+    """--sweep: the T sweep alone, one JSON line per point."""
+    import torch
+    from transformer_attention_fwd_gb300 import build as b
+    b.build()
+    from transformer_attention_fwd_gb300 import attn
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.fill_(1)  # noqa: E731
+    for pt in sweep_points(attn, max(5, min(args.steps, 200)), max(3, args.warmup), flush):
+        print(json.dumps(pt), flush=True)
     return 0
 
 

@@ -145,11 +145,17 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
  * allocator up front (a driver allocation in the middle of a decode step could
  * then fail with out-of-memory), or that keep allocation, and the
  * synchronisation it may bring, out of a latency-critical decode step.  This
- * call computes exactly what attn_fwd_decode computes, with the same
- * arguments and errors, but writes the split partials into a fixed workspace
- * that is part of the library's device image: an 8 MiB array that every GPU
- * loading libattn.so holds until the process exits.  It calls no cudaMalloc,
- * cudaFree or other allocating routine.
+ * call takes the arguments of attn_fwd_decode and computes the same
+ * attention, but writes the split partials into a fixed workspace that is
+ * part of the library's device image: an 8 MiB array that every GPU loading
+ * libattn.so holds until the process exits.  It calls no cudaMalloc, cudaFree
+ * or other allocating routine.  Its results are bit-identical to
+ * attn_fwd_decode's while the kernels are the same ones (automatic mode while
+ * the stream-K fragments fit, and explicit split counts whose partials fit);
+ * where it has to take the split kernel instead (larger shapes, below) they
+ * agree within the split path's float32 rounding.  Beyond attn_fwd_decode's
+ * errors it returns ATTN_ERR_UNSUPPORTED for an explicit num_splits whose
+ * partials do not fit the array.
  *
  * Automatic mode (num_splits = 0) runs the kernels attn_fwd_decode picks.
  * For MHA (Hq == Hkv) that is the split kernel (next paragraph); otherwise
@@ -168,7 +174,10 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
  * before reading it, so nothing has to start at zero; but calls whose kernels
  * can run at the same time on the GPU (e.g. on two streams with no ordering
  * between them) race on the array and give undefined results.  Order such
- * calls, e.g. issue them on one stream.
+ * calls, e.g. issue them on one stream.  After attn_get_device_status reports
+ * ATTN_ERR_TIMEOUT for a call, its outputs may also hold data that earlier
+ * calls left in the array (a kernel that gave up early leaves some partial
+ * slots unwritten, and the combine step reads them).
  *
  * Set-up: the first call on each device looks up the array's device address
  * once (cudaGetSymbolAddress, with that device current).  Make that first call

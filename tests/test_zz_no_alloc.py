@@ -12,10 +12,12 @@ has already run every other test.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, to_dev
+import oracle
+from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, compare, to_dev
 from transformer_attention_fwd_gb300.inputs import make_qkv
 
 pytestmark = pytest.mark.gpu
@@ -112,3 +114,63 @@ def test_noalloc_automatic_mode_uses_stream_k_while_it_fits(B, expect_stream):
         assert grid == B * Hkv and items >= 1
         assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
         assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tk,D,splits", [
+    (16, 32, 8, 4096, 128, 0),   # automatic mode: stream-K, fragments in the array
+    (4, 12, 4, 3001, 64, 5),     # explicit count: the split kernel, partials in the array
+])
+def test_noalloc_decode_matches_the_oracle(B, Hq, Hkv, Tk, D, splits):
+    """Each of the two kernels this entry point runs, compared directly with
+    the float64 oracle on the same bf16 inputs."""
+    a, fn = _noalloc()
+    qc, kc, vc = make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=50 + D)
+    q, k, v = to_dev(qc, kc, vc)
+    st, o, lse = _call(fn, q, k, v, splits)
+    assert st == a.ATTN_OK, a.last_error()
+    _, items, _ = a.last_launch_info()
+    check_status(a)
+    assert (items == 0) == (splits == 0)  # stream-K reports no split count
+    o_ref, lse_ref = oracle.attention_f64(qc, kc, vc, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, f"noalloc splits={splits}")
+
+
+def _randn_dev(shape, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return torch.randn(shape, generator=g, device="cuda", dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,Tk,lowered", [
+    (32, 8192, False),   # automatic count (4 splits) fits the array as chosen
+    (128, 1024, True),   # automatic count needs more than 8 MiB: lowered until it fits
+])
+def test_noalloc_automatic_mode_for_mha_uses_the_array(B, Tk, lowered):
+    """MHA (Hq == Hkv) in automatic mode runs the split kernel with more than
+    one split, so its partials live in the static array; where the count
+    attn_fwd_decode would choose does not fit, the count is lowered."""
+    a, fn = _noalloc()
+    Hq = Hkv = 32
+    D = 128
+    q = _randn_dev((B, Hq, 1, D), 60 + B)
+    k = _randn_dev((B, Hkv, Tk, D), 61 + B)
+    v = _randn_dev((B, Hkv, Tk, D), 62 + B)
+    o_ref, lse_ref = a.attn_fwd_decode(q, k, v)
+    _, splits_ref, _ = a.last_launch_info()
+    check_status(a)
+    ref_bytes = B * Hq * splits_ref * (D + 1) * 4
+    assert splits_ref > 1
+    assert (ref_bytes > SCRATCH_BYTES) == lowered, (splits_ref, ref_bytes)
+    for call in range(2):  # twice: the array keeps the first call's partials
+        st, o, lse = _call(fn, q, k, v, 0)
+        assert st == a.ATTN_OK, a.last_error()
+        _, splits, _ = a.last_launch_info()
+        check_status(a)
+        assert 1 < splits <= splits_ref
+        assert B * Hq * splits * (D + 1) * 4 <= SCRATCH_BYTES
+        if lowered:
+            assert splits < splits_ref
+            assert (o.float() - o_ref.float()).abs().max().item() <= TOL_O_BF16
+            assert (lse - lse_ref).abs().max().item() <= TOL_LSE_BF16
+        else:  # the same kernels with the same split count: equal bits
+            assert splits == splits_ref
+            assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
