@@ -59,6 +59,22 @@ def test_llama3_prefill_full(name, seed):
     compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, f"{name} seed {seed}")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tk,D,causal", [
+    (1, 4, 4, 4096, 4096, 64, False),   # 32 key tiles per work item
+    (2, 8, 2, 2048, 2048, 64, True),    # GQA, many items per CTA
+    (3, 6, 3, 1000, 1777, 64, True),    # Tq < Tk: limits cross 32-key chunks
+])
+def test_d64_longer_sequences(B, Hq, Hkv, Tq, Tk, D, causal):
+    """Head dim 64 runs two CTAs per SM on one query tile each; longer key
+    walks and several items per CTA cycle every pipeline barrier."""
+    a = attn()
+    q, k, v = make_qkv(B, Hq, Hkv, Tq, Tk, D, "bf16", seed=Tq + Tk)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=causal)
+    check_status(a)
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, causal)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
+
+
 def test_prefill_output_guard_bands():
     """Writes stay inside O and lse: sentinel margins around both are untouched."""
     a = attn()

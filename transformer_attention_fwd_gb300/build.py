@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libattn.so")
 
-SOURCES = ["attn_api.cu", "prefill_bf16.cu", "decode_bf16.cu", "simt_f32.cu", "varlen_sched.cu"]
+SOURCES = ["attn_api.cu", "prefill_bf16.cu", "prefill_d64.cu", "decode_bf16.cu", "simt_f32.cu",
+           "varlen_sched.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -41,6 +41,11 @@ cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse
                                 const Shape& s, const LaunchEnv& env, int* grid_out,
                                 int* items_out, int* kernels_launched);
 int prefill_block_rows();  // query rows per CTA work item
+// Dense prefill at head dim 64 (two CTAs per SM, one 128-row query tile per
+// work item); launch_prefill_bf16 routes D = 64 here.
+cudaError_t launch_prefill_d64(const PrefillMaps& maps, uint16_t* o, float* lse, const Shape& s,
+                               const LaunchEnv& env, int* grid_out, int* items_out,
+                               int* kernels_launched);
 
 // Packed variable-length prefill: q [total_q, Hq, D], k and v [total_k, Hkv,
 // D], sequence b at rows cu_q[b] .. cu_q[b+1]-1 of q and cu_k[b] ..
