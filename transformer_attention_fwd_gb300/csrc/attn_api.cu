@@ -233,6 +233,10 @@ attn_status run_prefill(const void* q, const void* k, const void* v, void* o, fl
     if (st != ATTN_OK) return st;
     st = make_map(v, s.Tk, static_cast<long long>(s.B) * s.Hkv, s.D, box, 3, &maps.v, false, f16);
     if (st != ATTN_OK) return st;
+    if (s.D == 64) {  // the head-dim-64 kernel stores O through TMA, 32 rows per warp
+        st = make_map(o, s.Tq, static_cast<long long>(s.B) * s.Hq, s.D, 32, 3, &maps.o, false, f16);
+        if (st != ATTN_OK) return st;
+    }
     int grid = 0, items = 0, kernels = 0;
     cudaError_t e = launch_prefill_bf16(maps, static_cast<uint16_t*>(o), lse, s, env, &grid,
                                         &items, &kernels);

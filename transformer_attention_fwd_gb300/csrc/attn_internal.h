@@ -36,6 +36,7 @@ cudaError_t launch_simt_f32(const float* q, const float* k, const float* v, floa
 // Prefill on tensor cores.  Tensor maps are built by the caller.
 struct PrefillMaps {
     CUtensorMap q, k, v;
+    CUtensorMap o;  // head dim 64 only: O as [B*Hq][Tq][D], box 64 x 32 rows (one warp's rows)
 };
 cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse,
                                 const Shape& s, const LaunchEnv& env, int* grid_out,

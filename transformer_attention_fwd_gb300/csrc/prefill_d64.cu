@@ -34,6 +34,9 @@
 //   warp 2      tensor-memory allocator
 //   warps 4-7   softmax and epilogue: warp w owns TMEM lane quarter w % 4,
 //               one query row per thread, all 128 keys of a tile in registers
+// The producers pull the next item's first Q, K and V tiles into L2 while the
+// current item runs.  The epilogue stages each warp's 32 rows of O in the
+// item's Q buffer and writes them with one TMA store.
 //
 // Softmax per tile, per row (base 2, x = s * scale * log2 e): the row maximum
 // of the tile's visible scores is taken every tile; the running reference m
@@ -165,6 +168,13 @@ __device__ void producer_qk(const CUtensorMap* tmQ, const CUtensorMap* tmK, uint
         mbar_arrive_expect_tx(&bars->q_full[qs], kTileBytes);
         tma_load_3d(smem + kQOff + qs * kTileBytes, tmQ, &bars->q_full[qs], 0, it.qt * BM, it.bh);
         ++q_it;
+        // Pull the next item's Q and first K tile into L2 meanwhile.
+        const int nx_idx = snake_item(k + 1, p.n_items);
+        if (nx_idx >= 0) {
+            const Item nx = decode_item(nx_idx, p);
+            tma_prefetch_l2_3d(tmQ, 0, nx.qt * BM, nx.bh);
+            tma_prefetch_l2_3d(tmK, 0, nx.lo * BN, nx.bkv);
+        }
         for (int j = it.lo; j < it.n; ++j, ++k_it) {
             const int s = k_it % kKStages;
             if (k_it >= (uint32_t)kKStages &&
@@ -190,6 +200,11 @@ __device__ void producer_v(const CUtensorMap* tmV, uint8_t* smem, Bars* bars, co
         const int idx = snake_item(k, p.n_items);
         if (idx < 0) continue;
         const Item it = decode_item(idx, p);
+        const int nx_idx = snake_item(k + 1, p.n_items);
+        if (nx_idx >= 0) {  // the next item's first V tile into L2 meanwhile
+            const Item nx = decode_item(nx_idx, p);
+            tma_prefetch_l2_3d(tmV, 0, nx.lo * BN, nx.bkv);
+        }
         for (int j = it.lo; j < it.n; ++j, ++v_it) {
             const int s = v_it % kVStages;
             if (v_it >= (uint32_t)kVStages &&
@@ -255,7 +270,6 @@ __device__ void mma_issuer(uint8_t* smem, Bars* bars, uint32_t tmem, const Param
             issue_qk<D, kF16>(tmem + kColS, q_desc, desc_advance(k_desc0, ks * kTile16), leader);
             mma_commit(&bars->s_full, leader);
             mma_commit(&bars->k_empty[ks], leader);
-            if (j == it.n - 1) mma_commit(&bars->q_empty[qs], leader);
             ++k_it;
             ++s_cnt;
             if (pending && !issue_pending_pv()) goto drain;
@@ -310,7 +324,8 @@ __device__ __forceinline__ void chunk_exp2(const uint32_t* s, uint64_t sc2, uint
 // the weights P and release them to the MMA warp.  Per item: the epilogue
 // O / sum -> 16-bit output and lse.
 template <bool kF16>
-__device__ void softmax_rows(Bars* bars, uint32_t tmem, const Params& p, const WaitGuard& g) {
+__device__ void softmax_rows(uint8_t* smem, const CUtensorMap* tmO, Bars* bars, uint32_t tmem,
+                             const Params& p, const WaitGuard& g) {
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int quarter = warp & 3;
@@ -318,7 +333,7 @@ __device__ void softmax_rows(Bars* bars, uint32_t tmem, const Params& p, const W
     const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     const bool win = p.window > 0;
     const int off = p.Tk - p.Tq;
-    uint32_t s_cnt = 0, pv_cnt = 0;
+    uint32_t s_cnt = 0, pv_cnt = 0, q_it = 0;
 
     for (int k = 0; k * static_cast<int>(gridDim.x) < p.n_items; ++k) {
         const int idx = snake_item(k, p.n_items);
@@ -351,27 +366,39 @@ __device__ void softmax_rows(Bars* bars, uint32_t tmem, const Params& p, const W
 
             // Chunk classes for the whole warp: 0 = no row sees a key of the
             // chunk, 2 = every row sees all of them, 1 = mask element-wise.
-            int cls[4];
+            // Only tiles that cross some row's limit (the diagonal, the end of
+            // the keys, a window's start) are classified at all.
+            const int key0 = j * BN;
+            int cls[4] = {2, 2, 2, 2};
+            float mx;
+            if (!(key0 + BN - 1 <= lim_lo && key0 >= lft_hi)) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int kc = j * BN + 32 * c;
-                const bool none = kc > lim_hi || kc + 31 < lft_lo;
-                const bool all = kc + 31 <= lim_lo && kc >= lft_hi;
-                cls[c] = none ? 0 : (all ? 2 : 1);
-            }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t* sc = &s[c >> 1][32 * (c & 1)];
-                if (cls[c] == 1) {
-                    const int kc = j * BN + 32 * c;
-                    const int dr = lim - kc;             // last visible offset in the chunk
-                    const int dl = win ? lft - kc : -1;  // first visible offset
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (e > dr || e < dl) sc[e] = __float_as_uint(-INFINITY);
+                for (int c = 0; c < 4; ++c) {
+                    const int kc = key0 + 32 * c;
+                    const bool none = kc > lim_hi || kc + 31 < lft_lo;
+                    const bool all = kc + 31 <= lim_lo && kc >= lft_hi;
+                    cls[c] = none ? 0 : (all ? 2 : 1);
                 }
-                if (cls[c] != 0) mx = fmaxf(mx, chunk_max(sc));
+                mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t* sc = &s[c >> 1][32 * (c & 1)];
+                    if (cls[c] == 1) {
+                        // Keep this a branch: executed on every tile as
+                        // selects, the masking would cost every tile.
+                        asm volatile("" ::: "memory");
+                        const int kc = key0 + 32 * c;
+                        const int dr = lim - kc;             // last visible offset in the chunk
+                        const int dl = win ? lft - kc : -1;  // first visible offset
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (e > dr || e < dl) sc[e] = __float_as_uint(-INFINITY);
+                    }
+                    if (cls[c] != 0) mx = fmaxf(mx, chunk_max(sc));
+                }
+            } else {
+                mx = fmaxf(fmaxf(chunk_max(&s[0][0]), chunk_max(&s[0][32])),
+                           fmaxf(chunk_max(&s[1][0]), chunk_max(&s[1][32])));
             }
 
             // Reference: the first tile sets it to the row maximum; later tiles
@@ -450,33 +477,49 @@ __device__ void softmax_rows(Bars* bars, uint32_t tmem, const Params& p, const W
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_free);  // the next item's P.V may overwrite O
-        if (row < p.Tq) {
-            const float inv = 1.0f / lr;
-            const int64_t orow = static_cast<int64_t>(it.bh) * p.Tq + row;
-            uint4* optr = reinterpret_cast<uint4*>(p.o + orow * D);
+        // The item's Q stage is free (its last QK^T completed before the last
+        // P.V): this warp's 32 rows are staged there in the tensor map's
+        // 128-byte-swizzled layout (16-byte chunk c of row r at c ^ (r % 8))
+        // and written out by one TMA store, which leaves out rows past Tq.
+        const int qs = q_it % kQStages;
+        ++q_it;
+        uint8_t* stage = smem + kQOff + qs * kTileBytes + 32 * quarter * 128;
+        const float inv = 1.0f / lr;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                uint4 w;
-                w.x = Elem16<kF16>::pack(__uint_as_float(ov[8 * v + 0]) * inv,
-                                         __uint_as_float(ov[8 * v + 1]) * inv);
-                w.y = Elem16<kF16>::pack(__uint_as_float(ov[8 * v + 2]) * inv,
-                                         __uint_as_float(ov[8 * v + 3]) * inv);
-                w.z = Elem16<kF16>::pack(__uint_as_float(ov[8 * v + 4]) * inv,
-                                         __uint_as_float(ov[8 * v + 5]) * inv);
-                w.w = Elem16<kF16>::pack(__uint_as_float(ov[8 * v + 6]) * inv,
-                                         __uint_as_float(ov[8 * v + 7]) * inv);
-                optr[v] = w;
-            }
-            if (p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * kLn2;
+        for (int c = 0; c < 8; ++c) {
+            uint4 w;
+            w.x = Elem16<kF16>::pack(__uint_as_float(ov[8 * c + 0]) * inv,
+                                     __uint_as_float(ov[8 * c + 1]) * inv);
+            w.y = Elem16<kF16>::pack(__uint_as_float(ov[8 * c + 2]) * inv,
+                                     __uint_as_float(ov[8 * c + 3]) * inv);
+            w.z = Elem16<kF16>::pack(__uint_as_float(ov[8 * c + 4]) * inv,
+                                     __uint_as_float(ov[8 * c + 5]) * inv);
+            w.w = Elem16<kF16>::pack(__uint_as_float(ov[8 * c + 6]) * inv,
+                                     __uint_as_float(ov[8 * c + 7]) * inv);
+            *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (wrow0 < p.Tq) {
+                tma_store_3d(tmO, stage, 0, wrow0, it.bh);
+                bulk_commit_group();
+                bulk_wait_group_read0();  // the stage may take the next Q once read out
+            }
+            mbar_arrive(&bars->q_empty[qs]);
+        }
+        if (row < p.Tq && p.lse != nullptr)
+            p.lse[static_cast<int64_t>(it.bh) * p.Tq + row] = (m + __log2f(l)) * kLn2;
     }
+    if (lane == 0) bulk_wait_group0();  // the last stores have landed
 }
 
 template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmO, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
@@ -485,7 +528,7 @@ prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&bars->q_full[s], 1);
-            mbar_init(&bars->q_empty[s], 1);
+            mbar_init(&bars->q_empty[s], 4);  // the four softmax warps' O stores
         }
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
@@ -508,6 +551,7 @@ prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 2) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -530,7 +574,7 @@ prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
     } else {
         regs_increase<kSoftmaxRegs>();
-        softmax_rows<kF16>(bars, tmem, p, g);
+        softmax_rows<kF16>(smem, &tmO, bars, tmem, p, g);
     }
 
     tc_fence_before_sync();
@@ -557,7 +601,8 @@ cudaError_t launch(const PrefillMaps& maps, const Params& prm, int grid, cudaStr
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    prefill_d64_kernel<kF16><<<grid, kThreads, kSmemBytes, stream>>>(maps.q, maps.k, maps.v, prm);
+    prefill_d64_kernel<kF16><<<grid, kThreads, kSmemBytes, stream>>>(maps.q, maps.k, maps.v, maps.o,
+                                                                      prm);
     return cudaGetLastError();
 }
 
