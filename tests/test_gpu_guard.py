@@ -36,11 +36,13 @@ def test_decode_writes_stay_inside(splits):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 
 
-def test_paged_decode_writes_stay_inside():
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 64), (16, 8, 128)])
+def test_paged_decode_writes_stay_inside(Hq, Hkv, D):
     a = attn()
-    q, kv, bt, sl = (x.cuda() for x in make_paged(5, 8, 2, 64, 16, [300, 0, 17, 1000, 1], seed=142))
+    q, kv, bt, sl = (x.cuda() for x in make_paged(5, Hq, Hkv, D, 16, [300, 0, 17, 1000, 1],
+                                                  seed=142))
     ob, o = _guarded(q.shape, torch.bfloat16, 7.0)
-    lb, lse = _guarded((5, 8), torch.float32, 7.0)
+    lb, lse = _guarded((5, Hq), torch.float32, 7.0)
     a.attn_fwd_decode_paged(q, kv, bt, sl, out=o, lse=lse)
     check_status(a)
     assert _margins_intact(ob, 7.0) and _margins_intact(lb, 7.0)

@@ -39,6 +39,11 @@ def _check(a, q, kv, bt, sl, what):
     (3, 4, 2, 64, 1, [3, 40, 7]),                 # one token per block
     (2, 8, 2, 128, 256, [700, 256]),              # large blocks
     (2, 16, 2, 64, 16, [100, 2000]),              # eight heads per KV head, D=64
+    (2, 8, 4, 128, 32, [700, 33]),                # 32-token blocks, lengths off the block size
+    (3, 16, 8, 128, 8, [1000, 9, 64]),            # 8-token blocks: eight pages per 64-key chunk
+    (2, 8, 8, 128, 16, [300, 4096]),              # MHA in 16-token blocks
+    (2, 32, 8, 64, 16, [777, 2048]),              # D=64, GQA-4
+    (2, 8, 4, 64, 32, [500, 31]),                 # D=64, 32-token blocks
 ])
 def test_paged_matches_oracle(B, Hq, Hkv, D, page, lens):
     a = attn()
@@ -53,6 +58,16 @@ def test_many_short_requests():
     lens = rng.integers(1, 200, size=96)
     q, kv, bt, sl = make_paged(96, 4, 4, 64, 16, lens, seed=12)
     _check(a, q, kv, bt, sl, "96 short requests")
+
+
+def test_many_short_requests_gqa():
+    """Short GQA requests in 16-token pages: slices start and end inside pages
+    and units of several requests share a CTA."""
+    a = attn()
+    rng = np.random.default_rng(17)
+    lens = rng.integers(1, 200, size=80)
+    q, kv, bt, sl = make_paged(80, 16, 8, 128, 16, lens, seed=17)
+    _check(a, q, kv, bt, sl, "80 short GQA requests")
 
 
 @pytest.mark.parametrize("seed", [0, 1])
