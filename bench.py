@@ -5,7 +5,7 @@ One step = one causal GQA prefill forward of the Llama-3-8B-shaped workload
 (B=1, Hq=32, Hkv=8, T=8192, D=128, bf16 I/O), through libattn.so's C ABI on
 inputs already resident in HBM.  The same run also times, under "secondary":
 the stream-K decode (B=64, Hq=32, Hkv=8, Tk=4096, D=128) on a dense and on a
-paged cache, the GPT-2-small-shaped prefill (B=8, H=12, T=1024, D=64), the
+paged cache, the decode with eight query heads per KV head (B=32, Hq=64), the GPT-2-small-shaped prefill (B=8, H=12, T=1024, D=64), the
 T=4096 non-causal prefill, the T=8192 prefill with a 4096-key sliding window
 and with fp16 I/O, and a packed batch of 32 sequences of 128..8192 tokens.
 
@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 METRIC = "attn fwd TFLOP/s (causal prefill) & decode KV GB/s, % of GB300 roofline"
 PRIMARY = "llama3_8b_prefill_bf16_b1_hq32_hkv8_t8192_d128_causal"
 DECODE = "gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128"
+GQA8_DECODE = "gqa8_decode_bf16_b32_hq64_hkv8_tk4096_d128"
 PAGED_DECODE = "gqa_paged_decode_bf16_b64_hq32_hkv8_tk4096_d128_p16"
 GPT2 = "gpt2s_prefill_bf16_b8_h12_t1024_d64_causal"
 VARLEN = "llama3_8b_varlen_prefill_bf16_32seq_len128to8192_hq32_hkv8_d128_causal"
@@ -40,9 +41,14 @@ L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 PREFILL_SOURCES = ["transformer_attention_fwd_gb300/csrc/prefill_bf16.cu",
+                   "transformer_attention_fwd_gb300/csrc/prefill_common.cuh",
                    "transformer_attention_fwd_gb300/csrc/sm100.cuh"]
+PREFILL_D64_SOURCES = ["transformer_attention_fwd_gb300/csrc/prefill_d64.cu",
+                       "transformer_attention_fwd_gb300/csrc/prefill_common.cuh",
+                       "transformer_attention_fwd_gb300/csrc/sm100.cuh"]
 DECODE_SOURCES = ["transformer_attention_fwd_gb300/csrc/decode_bf16.cu",
                   "transformer_attention_fwd_gb300/csrc/sm100.cuh"]
+VARLEN_SOURCES = PREFILL_SOURCES + ["transformer_attention_fwd_gb300/csrc/varlen_sched.cu"]
 
 
 def parse_args():
@@ -403,6 +409,29 @@ def run_secondary(args, attn, peaks, flush):
                      "note": "step time includes the stream kernel and the fragment combine kernel"},
     }
     del q, k, v, o, lse
+    # Eight query heads per KV head: automatic mode runs the tensor-core
+    # prefill kernel over the query-head groups.
+    w = WORKLOADS[GQA8_DECODE]
+    q, k, v = (x.cuda() for x in make_workload(w, 0))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device="cuda")
+    fn = lambda: attn.attn_fwd(q, k, v, causal=False, out=o, lse=lse)  # noqa: E731
+    fn()
+    _, items, kernels = attn.last_launch_info()
+    times = time_steps(fn, steps, 5)
+    ms = sum(times) / steps
+    gbs = w.io_bytes() / (ms * 1e-3) / 1e9
+    out["gqa8_decode"] = {
+        "workload": GQA8_DECODE, "value": round(gbs, 1), "unit": "GB/s",
+        "ms_per_step": round(ms, 5), "algorithmic_bytes": w.io_bytes(),
+        "mode": f"tensor-core prefill kernel over the query-head groups, {items} work items",
+        "kernels_per_step": kernels,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gbs / hbm, 4),
+                     "traffic": load_traffic("gqa8_decode_b32_tk4096", PREFILL_SOURCES),
+                     "note": "K+V (537 MB) exceed L2; no flush needed"},
+    }
+    del q, k, v, o, lse
     # The same decode against a paged cache (16-token blocks in a random order).
     from transformer_attention_fwd_gb300.inputs import PAGED_WORKLOADS, make_paged_workload
     pw = PAGED_WORKLOADS[PAGED_DECODE]
@@ -420,7 +449,8 @@ def run_secondary(args, attn, peaks, flush):
         "ms_per_step": round(ms, 5), "algorithmic_bytes": pw.io_bytes(),
         "kernels_per_step": kernels,
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gbs / hbm, 4), "traffic": None,
+                     "frac": round(gbs / hbm, 4),
+                     "traffic": load_traffic("paged_decode_b64_tk4096_p16", DECODE_SOURCES),
                      "note": "step time includes the length prefix, stream and combine kernels"},
     }
     del q, kv, bt, sl, o, lse
@@ -437,7 +467,8 @@ def run_secondary(args, attn, peaks, flush):
     out["gpt2s_prefill"] = {
         "workload": GPT2, "value": round(tf, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "traffic": load_traffic("prefill_gpt2s_d64", PREFILL_D64_SOURCES)},
     }
     # Non-causal T=4096 variant of the primary workload.
     w = WORKLOADS["llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_noncausal"]
@@ -450,7 +481,8 @@ def run_secondary(args, attn, peaks, flush):
     out["llama3_noncausal_t4096"] = {
         "workload": w.name, "value": round(tf, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "traffic": load_traffic("prefill_llama3_t4096_noncausal", PREFILL_SOURCES)},
     }
     # Sliding window of 4096 keys on the primary workload's shapes.
     w = WORKLOADS[PRIMARY]
@@ -466,7 +498,8 @@ def run_secondary(args, attn, peaks, flush):
         "workload": f"{PRIMARY}_window{W}", "value": round(tf, 3), "unit": "TFLOP/s",
         "ms_per_step": round(ms, 5), "flops_per_step": 4.0 * pairs * w.D * w.B * w.Hq,
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None},
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "traffic": load_traffic("prefill_llama3_t8192_window4096", PREFILL_SOURCES)},
     }
     del q, k, v, o
     # The primary workload with fp16 I/O.
@@ -480,7 +513,8 @@ def run_secondary(args, attn, peaks, flush):
         "workload": PRIMARY.replace("bf16", "f16"), "value": round(tf, 3), "unit": "TFLOP/s",
         "ms_per_step": round(ms, 5),
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "traffic": load_traffic("prefill_llama3_t8192_f16", PREFILL_SOURCES),
                      "note": "fp16 and bf16 share the measured dense peak"},
     }
     del q, k, v, o
@@ -500,7 +534,8 @@ def run_secondary(args, attn, peaks, flush):
         "workload": VARLEN, "value": round(tf, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
         "flops_per_step": vw.flops(), "tokens": int(q.shape[0]), "kernels_per_step": kernels,
         "roofline": {"bound": "tensor", "achieved": round(tf, 3), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "traffic": load_traffic("prefill_varlen_mix", VARLEN_SOURCES),
                      "note": "step time includes the two scheduling kernels"},
     }
     del q, k, v, cq, ck, o, lse

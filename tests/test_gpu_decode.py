@@ -54,3 +54,49 @@ def test_decode_shapes(B, Hq, Hkv, Tk, D, splits):
     check_status(a)
     o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
     compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_gqa8_decode_full(seed):
+    """B=32, Hq=64, Hkv=8, Tk=4096, D=128 (eight query heads per KV head):
+    automatic mode runs the tensor-core prefill kernel on the query-head
+    groups (one work item per (b, hkv)); every output compared."""
+    a = attn()
+    w = WORKLOADS["gqa8_decode_bf16_b32_hq64_hkv8_tk4096_d128"]
+    q, k, v = make_workload(w, seed)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=False)
+    _, items, kernels = a.last_launch_info()
+    check_status(a)
+    assert items == w.B * w.Hkv and kernels == 1
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, w.name)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tk,D,dtype", [
+    (8, 64, 8, 1000, 128, "bf16"),    # B*Hq = 512: the smallest shape routed to the prefill kernel
+    (4, 128, 8, 3001, 64, "bf16"),    # sixteen heads per KV head, D=64 (two CTAs per SM)
+    (16, 32, 2, 513, 128, "bf16"),
+    (8, 64, 8, 700, 128, "f16"),
+    (1, 512, 1, 2048, 128, "bf16"),   # MQA with 512 query heads: one item of 512 rows
+])
+def test_many_heads_per_kv_head_decode(B, Hq, Hkv, Tk, D, dtype):
+    a = attn()
+    q, k, v = make_qkv(B, Hq, Hkv, 1, Tk, D, dtype, seed=Tk + Hq)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=False)
+    _, items, _ = a.last_launch_info()
+    check_status(a)
+    assert items == B * Hkv * -(-(Hq // Hkv) // (128 if D == 64 else 256))
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
+
+
+def test_prefill_route_agrees_with_split_kernel():
+    """The two decode kernels for eight heads per KV head agree (an explicit
+    split count keeps the CUDA-core split kernel)."""
+    a = attn()
+    q, k, v = to_dev(*make_qkv(8, 64, 8, 1, 2500, 128, "bf16", seed=9))
+    o1, l1 = a.attn_fwd_decode(q, k, v)
+    o2, l2 = a.attn_fwd_decode(q, k, v, num_splits=4)
+    check_status(a)
+    assert (o1.float() - o2.float()).abs().max().item() <= 8e-3
+    assert (l1 - l2).abs().max().item() <= 5e-5

@@ -275,9 +275,34 @@ attn_status run_decode_stream(const void* q, const void* k, const void* v, void*
 // query heads per KV head on, stream-K is ahead.  (fp16 has only stream-K.)
 bool decode_prefers_split_kernel(const Shape& s) { return s.Hq == s.Hkv && !s.f16; }
 
+// Automatic decode with many query heads per KV head runs on the tensor-core
+// prefill kernel: the group of query heads that share K/V head (b, hkv) is a
+// block of Tq = group query rows against Tk keys, non-causal, so with Q
+// viewed as [B, Hkv, group, D] (the same memory) the decode is a prefill of
+// B*Hkv heads.  The CUDA-core kernels spend 2*group*D multiply-adds per K/V
+// row and are bound by instruction issue from group 8 on (about 3 TB/s at 8,
+// 1.2 TB/s at 16), while the prefill streams one (b, hkv) per SM at about
+// 42 GB/s each.  Same-process A/B, GB/s, CUDA-core -> prefill kernel (Hkv 8,
+// Tk 4096, D 128): group 8 at B = 4, 8, 16, 32: 1490 -> 1361, 2083 -> 2724,
+// 2651 -> 4375, 2985 -> 4873; group 4 at B = 64: 5879 -> 5409.  Hence: from
+// 8 heads per KV head on, once B * Hq >= 512 query rows.
+bool decode_prefers_prefill_kernel(const Shape& s, int /*num_sms*/) {
+    const int group = s.Hq / s.Hkv;
+    return group >= 8 && static_cast<long long>(s.B) * s.Hq >= 512;
+}
+
+attn_status run_decode_as_prefill(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, const Shape& s, const LaunchEnv& env) {
+    Shape p{s.B, s.Hkv, s.Hkv, s.Hq / s.Hkv, s.Tk, s.D, 0, s.scale};
+    p.f16 = s.f16;
+    return run_prefill(q, k, v, o, lse, p, env);
+}
+
 attn_status run_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                        const Shape& s, int num_splits, const LaunchEnv& env) {
     if (num_splits == 0) {
+        if (decode_prefers_prefill_kernel(s, env.num_sms))
+            return run_decode_as_prefill(q, k, v, o, lse, s, env);
         if (!decode_prefers_split_kernel(s)) return run_decode_stream(q, k, v, o, lse, s, env);
         num_splits = decode_choose_splits(s, env.num_sms);
     }
@@ -804,6 +829,8 @@ extern "C" attn_status attn_fwd_decode_noalloc(const void* q, const void* k, con
     st = device_env(stream, &env);
     if (st != ATTN_OK) return st;
     const Shape s{B, Hq, Hkv, 1, Tk, D, 0, scale};
+    if (num_splits == 0 && decode_prefers_prefill_kernel(s, env.num_sms))
+        return run_decode_as_prefill(q, k, v, o, lse, s, env);  // no workspace at all
     if (num_splits == 0 && !decode_prefers_split_kernel(s) &&
         decode_stream_workspace_bytes(s, env.num_sms) <= kNoAllocScratchBytes) {
         // Automatic mode: the stream-K kernels of attn_fwd_decode, their

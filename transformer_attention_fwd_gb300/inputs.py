@@ -68,6 +68,10 @@ WORKLOADS = {
         Workload("llama3_8b_prefill_bf16_b1_hq32_hkv8_t4096_d128_causal", 1, 32, 8, 4096, 4096, 128, True, "bf16"),
     "gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128":
         Workload("gqa_decode_bf16_b64_hq32_hkv8_tk4096_d128", 64, 32, 8, 1, 4096, 128, False, "bf16"),
+    # Eight query heads per KV head (a larger query-head group than the named
+    # decode workload's four; "3.3 Self-Attention机制深入理解" §9.3's group map).
+    "gqa8_decode_bf16_b32_hq64_hkv8_tk4096_d128":
+        Workload("gqa8_decode_bf16_b32_hq64_hkv8_tk4096_d128", 32, 64, 8, 1, 4096, 128, False, "bf16"),
 }
 
 
