@@ -592,8 +592,8 @@ def run_profile_case(args):
     from transformer_attention_fwd_gb300 import build as b
     b.build()
     from transformer_attention_fwd_gb300 import attn
-    from transformer_attention_fwd_gb300.inputs import (PAGED_WORKLOADS, WORKLOADS,
-                                                        make_paged_workload, make_workload)
+    from transformer_attention_fwd_gb300.inputs import (PAGED_WORKLOADS, WORKLOADS, make_paged_workload,
+                                                        make_qkv, make_workload)
     from transformer_attention_fwd_gb300.inputs import VARLEN_WORKLOADS, make_varlen_workload
     if args.profile_case in VARLEN_WORKLOADS:
         vw = VARLEN_WORKLOADS[args.profile_case]
@@ -617,11 +617,23 @@ def run_profile_case(args):
         print(json.dumps({"profile_case": pw.name, "ms_per_step": round(ms, 5),
                           "gbs": round(pw.io_bytes() / (ms * 1e-3) / 1e9, 1)}), flush=True)
         return 0
-    w = WORKLOADS[args.profile_case]
-    q, k, v = (x.cuda() for x in make_workload(w, 0))
+    # The primary workload's sliding-window and fp16 lines.
+    name, window, dtype = args.profile_case, 0, None
+    if name == PRIMARY + "_window4096":
+        name, window = PRIMARY, 4096
+    elif name == PRIMARY.replace("bf16", "f16"):
+        name, dtype = PRIMARY, "f16"
+    w = WORKLOADS[name]
+    if dtype is None:
+        q, k, v = (x.cuda() for x in make_workload(w, 0))
+    else:
+        q, k, v = (x.cuda() for x in make_qkv(w.B, w.Hq, w.Hkv, w.Tq, w.Tk, w.D, dtype, 0))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device="cuda")
-    fn = lambda: attn.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)  # noqa: E731
+    if window:
+        fn = lambda: attn.attn_fwd_window(q, k, v, window, out=o, lse=lse)  # noqa: E731
+    else:
+        fn = lambda: attn.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse)  # noqa: E731
     times = time_steps(fn, args.steps, args.warmup)
     st = attn.device_status()
     if st != attn.ATTN_OK:
