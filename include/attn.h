@@ -124,11 +124,15 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v,
  * CTA (a (b, hkv) cut by a slice boundary is merged the same way); for MHA
  * (Hq == Hkv) instead the split ranges below, their count chosen to fill the
  * last wave of CTAs (measured faster there).  With 8 or more query heads per
- * KV head and B*Hq >= 512, automatic mode instead runs the tensor-core
- * prefill kernel: the query heads that share a KV head are the rows of a
- * non-causal prefill against its keys (q viewed as [B, Hkv, Hq/Hkv, D]), with
- * no workspace and no split; P is rounded to bf16 for the tensor cores as in
- * attn_fwd_prefill.
+ * KV head, automatic mode instead runs the tensor-core prefill kernel: the
+ * query heads that share a KV head are the rows of a non-causal prefill
+ * against its keys (q viewed as [B, Hkv, Hq/Hkv, D]), P rounded to bf16 for
+ * the tensor cores as in attn_fwd_prefill.  For bf16 at D = 128, when the
+ * B*Hkv pairs fill at most half the SMs, each pair's keys are cut into
+ * ranges of at least two 128-key tiles, one work item each, whose partials
+ * are merged like the split ranges below (the range count is reported as
+ * attn_last_launch_info's items); otherwise one work item per pair, with no
+ * workspace, from B*Hq >= 512 query rows on.
  * 1..256 = that many equal ranges per (b, hkv) (clamped to the number of
  * keys).  The result does not depend on the split choice beyond float32
  * rounding.  Partial results live in a workspace the library allocates and
@@ -163,10 +167,12 @@ attn_status attn_fwd_decode(const void* q, const void* k, const void* v,
  * partials do not fit the array.
  *
  * Automatic mode (num_splits = 0) runs the kernels attn_fwd_decode picks.
- * With 8 or more query heads per KV head and B*Hq >= 512 that is the prefill
- * kernel, which needs no workspace.  For MHA (Hq == Hkv) it is the split
- * kernel (next paragraph); otherwise the stream-K kernels, whenever their
- * fragment workspace fits in the 8 MiB:
+ * With 8 or more query heads per KV head that is the prefill kernel, per
+ * (b, hkv) with no workspace, or over key ranges with their partials in the
+ * array (B*Hq*ranges*(D+1)*4 bytes; when that does not fit, the CUDA-core
+ * kernels below run instead).  For MHA (Hq == Hkv) it is the split kernel
+ * (next paragraph); otherwise the stream-K kernels, whenever their fragment
+ * workspace fits in the 8 MiB:
  * B*Hq*nseg*(D+1)*4 bytes (plus 256), where nseg = ceil(Tk / slice) + 1 and
  * slice = ceil(B*Hkv*(Hq/Hkv/hc)*Tk / SMs) keys, hc being the heads one CTA
  * serves (8, 4, 2 or 1, the largest that divides Hq/Hkv).  That holds for

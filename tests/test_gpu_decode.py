@@ -1,5 +1,6 @@
 """Split-KV decode parity against the float64 oracle."""
 import pytest
+import torch
 
 import oracle
 from gpu_util import TOL_LSE_BF16, TOL_O_BF16, attn, check_status, compare, to_dev
@@ -72,22 +73,51 @@ def test_gqa8_decode_full(seed):
     compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, w.name)
 
 
+def _group_route(B, Hq, Hkv, Tk, D, dtype, sms):
+    """The automatic decode route for 8 or more query heads per KV head, as
+    the library states it: key ranges on the prefill kernel (bf16, D=128,
+    (b, hkv) pairs filling at most half the SMs, two key tiles per range),
+    else the prefill kernel per (b, hkv) from B*Hq >= 512 rows on, else the
+    CUDA-core stream-K kernel."""
+    pairs, tiles = B * Hkv, -(-Tk // 128)
+    if dtype == "bf16" and D == 128 and 2 * pairs <= sms:
+        splits = min(sms // pairs, tiles // 2)
+        if splits >= 2:
+            per = -(-tiles // splits)
+            return "split", -(-tiles // per)
+    if B * Hq >= 512:
+        return "prefill", B * Hkv * -(-(Hq // Hkv) // (128 if D == 64 else 256))
+    return "stream", 0
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,Tk,D,dtype", [
-    (8, 64, 8, 1000, 128, "bf16"),    # B*Hq = 512: the smallest shape routed to the prefill kernel
-    (4, 128, 8, 3001, 64, "bf16"),    # sixteen heads per KV head, D=64 (two CTAs per SM)
-    (16, 32, 2, 513, 128, "bf16"),
-    (8, 64, 8, 700, 128, "f16"),
-    (1, 512, 1, 2048, 128, "bf16"),   # MQA with 512 query heads: one item of 512 rows
+    (8, 64, 8, 1000, 128, "bf16"),    # 64 pairs: two key ranges each
+    (4, 64, 8, 4096, 128, "bf16"),    # 32 pairs: four key ranges each
+    (2, 64, 8, 32768, 128, "bf16"),   # long keys, nine ranges
+    (1, 32, 1, 8192, 128, "bf16"),    # MQA, one pair: 32 ranges
+    (16, 32, 2, 513, 128, "bf16"),    # sixteen heads per KV head, a ragged last tile
+    (1, 512, 1, 2048, 128, "bf16"),   # 512 query heads: two query blocks per range
+    (16, 64, 8, 700, 128, "bf16"),    # 128 pairs: one item per (b, hkv)
+    (4, 128, 8, 3001, 64, "bf16"),    # D=64 (two CTAs per SM), one item per (b, hkv)
+    (8, 64, 8, 700, 128, "f16"),      # fp16: one item per (b, hkv)
+    (2, 64, 8, 1000, 128, "f16"),     # fp16 with few rows: the CUDA-core kernel
 ])
 def test_many_heads_per_kv_head_decode(B, Hq, Hkv, Tk, D, dtype):
     a = attn()
     q, k, v = make_qkv(B, Hq, Hkv, 1, Tk, D, dtype, seed=Tk + Hq)
     o, lse = a.attn_fwd(*to_dev(q, k, v), causal=False)
-    _, items, _ = a.last_launch_info()
+    _, items, kernels = a.last_launch_info()
     check_status(a)
-    assert items == B * Hkv * -(-(Hq // Hkv) // (128 if D == 64 else 256))
+    route, n = _group_route(B, Hq, Hkv, Tk, D, dtype,
+                            torch.cuda.get_device_properties(0).multi_processor_count)
+    if route == "split":
+        assert (items, kernels) == (n, 2)
+    elif route == "prefill":
+        assert (items, kernels) == (n, 1)
+    else:
+        assert items == 0
     o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
-    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, f"{route} route")
 
 
 def test_prefill_route_agrees_with_split_kernel():

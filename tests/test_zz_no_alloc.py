@@ -174,3 +174,27 @@ def test_noalloc_automatic_mode_for_mha_uses_the_array(B, Tk, lowered):
         else:  # the same kernels with the same split count: equal bits
             assert splits == splits_ref
             assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tk", [
+    (4, 64, 8, 4096),    # few (b, hkv) pairs: key ranges on the prefill kernel, partials in the array
+    (32, 64, 8, 1000),   # enough pairs: the prefill kernel per (b, hkv), no workspace at all
+])
+def test_noalloc_wide_groups_match_the_allocating_decode(B, Hq, Hkv, Tk):
+    """Eight query heads per KV head: automatic mode runs the same tensor-core
+    kernels as attn_fwd_decode (equal bits), twice in a row."""
+    a, fn = _noalloc()
+    D = 128
+    qc, kc, vc = make_qkv(B, Hq, Hkv, 1, Tk, D, "bf16", seed=70 + B)
+    q, k, v = to_dev(qc, kc, vc)
+    o_ref, lse_ref = a.attn_fwd_decode(q, k, v)
+    info_ref = a.last_launch_info()
+    check_status(a)
+    for call in range(2):
+        st, o, lse = _call(fn, q, k, v, 0)
+        assert st == a.ATTN_OK, a.last_error()
+        assert a.last_launch_info() == info_ref
+        check_status(a)
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    o64, lse64 = oracle.attention_f64(qc, kc, vc, False)
+    compare(o, lse, o64, lse64, TOL_O_BF16, TOL_LSE_BF16, "noalloc, eight heads per KV head")

@@ -298,9 +298,66 @@ attn_status run_decode_as_prefill(const void* q, const void* k, const void* v, v
     return run_prefill(q, k, v, o, lse, p, env);
 }
 
+// With few (b, hkv) the same prefill leaves SMs idle, so its keys are cut
+// into ranges: each (b, hkv, range) is one work item writing a normalised
+// partial output and its log-sum-exp, and the split decode's combine kernel
+// merges the ranges ("3.3 Self-Attention机制深入理解" §12.3).  Taken for bf16 at
+// D = 128 with 8 or more query heads per KV head when the (b, hkv) pairs fill
+// fewer than half the SMs and each range still holds two key tiles; returns
+// the range count (every range non-empty), or 1 when not taken.
+int decode_group_splits(const Shape& s, int num_sms) {
+    if (s.f16 || s.D != 128 || s.Hq / s.Hkv < 8) return 1;
+    const long long pairs = static_cast<long long>(s.B) * s.Hkv;
+    if (2 * pairs > num_sms) return 1;
+    const int tiles = (s.Tk + 127) / 128;
+    int splits = static_cast<int>(num_sms / pairs);
+    if (splits > tiles / 2) splits = tiles / 2;
+    if (splits < 2) return 1;
+    const int per = (tiles + splits - 1) / splits;
+    return (tiles + per - 1) / per;
+}
+
+size_t group_split_workspace_bytes(const Shape& s, int splits) {
+    return static_cast<size_t>(s.B) * s.Hq * splits * (s.D + 1) * sizeof(float);
+}
+
+// ws: group_split_workspace_bytes(s, splits) bytes of device memory.
+attn_status run_decode_as_split_prefill(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, const Shape& s, int splits, void* ws,
+                                        const LaunchEnv& env) {
+    Shape p{s.B, s.Hkv, s.Hkv, s.Hq / s.Hkv, s.Tk, s.D, 0, s.scale};
+    const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+    p.kv_splits = splits;
+    p.split_o = static_cast<float*>(ws);
+    p.split_lse = p.split_o + rows * splits * s.D;
+    attn_status st = run_prefill(q, k, v, o, lse, p, env);
+    if (st != ATTN_OK) return st;
+    const int grid = t_last_grid;
+    cudaError_t e = launch_decode_combine(p.split_o, p.split_lse, static_cast<uint16_t*>(o), lse,
+                                          static_cast<int>(rows), s.D, splits, env);
+    if (e != cudaSuccess) return cuda_fail(e, "decode combine launch");
+    record_launch(grid, splits, 2);
+    return ok();
+}
+
 attn_status run_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                        const Shape& s, int num_splits, const LaunchEnv& env) {
     if (num_splits == 0) {
+        const int ks = decode_group_splits(s, env.num_sms);
+        if (ks > 1) {
+            const size_t bytes = group_split_workspace_bytes(s, ks);
+            void* ws = nullptr;
+            cudaError_t e = cudaMallocAsync(&ws, bytes, env.stream);
+            if (e != cudaSuccess || ws == nullptr) {
+                cudaGetLastError();
+                return fail(ATTN_ERR_NO_MEMORY, "decode workspace of %zu bytes: %s", bytes,
+                            cudaGetErrorString(e));
+            }
+            attn_status st = run_decode_as_split_prefill(q, k, v, o, lse, s, ks, ws, env);
+            e = cudaFreeAsync(ws, env.stream);
+            if (st == ATTN_OK && e != cudaSuccess) return cuda_fail(e, "freeing the decode workspace");
+            return st;
+        }
         if (decode_prefers_prefill_kernel(s, env.num_sms))
             return run_decode_as_prefill(q, k, v, o, lse, s, env);
         if (!decode_prefers_split_kernel(s)) return run_decode_stream(q, k, v, o, lse, s, env);
@@ -829,8 +886,17 @@ extern "C" attn_status attn_fwd_decode_noalloc(const void* q, const void* k, con
     st = device_env(stream, &env);
     if (st != ATTN_OK) return st;
     const Shape s{B, Hq, Hkv, 1, Tk, D, 0, scale};
-    if (num_splits == 0 && decode_prefers_prefill_kernel(s, env.num_sms))
-        return run_decode_as_prefill(q, k, v, o, lse, s, env);  // no workspace at all
+    if (num_splits == 0) {
+        const int ks = decode_group_splits(s, env.num_sms);
+        if (ks > 1 && group_split_workspace_bytes(s, ks) <= kNoAllocScratchBytes) {
+            void* ws = nullptr;
+            st = noalloc_scratch(env.device, &ws);
+            if (st != ATTN_OK) return st;
+            return run_decode_as_split_prefill(q, k, v, o, lse, s, ks, ws, env);
+        }
+        if (ks == 1 && decode_prefers_prefill_kernel(s, env.num_sms))
+            return run_decode_as_prefill(q, k, v, o, lse, s, env);  // no workspace at all
+    }
     if (num_splits == 0 && !decode_prefers_split_kernel(s) &&
         decode_stream_workspace_bytes(s, env.num_sms) <= kNoAllocScratchBytes) {
         // Automatic mode: the stream-K kernels of attn_fwd_decode, their

@@ -25,6 +25,14 @@ struct Shape {
     float scale;
     int window = 0;  // > 0: sliding window of that many keys (causal, prefill kernel)
     int f16 = 0;     // 16-bit I/O is fp16 instead of bf16 (prefill and stream-K decode)
+    // D = 128 prefill kernel only, non-causal without window: > 1 cuts every
+    // head's keys into that many ranges; each writes its normalised partial
+    // output to split_o [B*Hq*Tq, splits, D] and its base-2 log-sum-exp to
+    // split_lse [B*Hq*Tq, splits] instead of O and lse (the split count is
+    // lowered so that no range is empty; the launcher reports it in items).
+    int kv_splits = 1;
+    float* split_o = nullptr;
+    float* split_lse = nullptr;
 };
 
 // Each launcher returns cudaSuccess or the CUDA error of its launch; argument
@@ -86,6 +94,10 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
                                uint16_t* o, float* lse, float* ws_o, float* ws_lse,
                                const Shape& s, int splits, const LaunchEnv& env,
                                int* kernels_launched);
+// The merge of split partials alone (ws_o [rows, splits, D], ws_lse [rows,
+// splits] base 2) into bf16 O and lse (may be null).
+cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16_t* o, float* lse,
+                                  int rows, int D, int splits, const LaunchEnv& env);
 int decode_choose_splits(const Shape& s, int num_sms);
 
 // Stream-K decode: one persistent CTA per SM over equal slices of all keys;

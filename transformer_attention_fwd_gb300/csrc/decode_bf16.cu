@@ -466,6 +466,16 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
     return e;
 }
 
+cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16_t* o, float* lse,
+                                  int rows, int D, int splits, const LaunchEnv& env) {
+    const size_t sh = static_cast<size_t>(splits) * sizeof(float);
+    if (D == 64)
+        decode_combine_kernel<64><<<rows, 64, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
+    else
+        decode_combine_kernel<128><<<rows, 128, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
+    return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // Stream-K decode (automatic mode).
 //

@@ -134,6 +134,14 @@ struct PrefillParams {
     const int4* items;
     const int* n_items_dev;
     int total_q;
+    // Key splits (dense mode, non-causal, no window): item idx covers key
+    // tiles [s * tiles_per_split, (s + 1) * tiles_per_split) of its head,
+    // s = idx % splits, and writes its normalised partial output (fp32
+    // [rows, splits, D]) and base-2 log-sum-exp ([rows, splits]) to ws_o and
+    // ws_lse instead of O and lse; a combine kernel merges the splits.
+    int splits, tiles_per_split;
+    float* ws_o;
+    float* ws_lse;
     unsigned* status;
     unsigned long long limit_ns;
 };
@@ -146,6 +154,7 @@ struct Item {
     int bh, qb, bkv;
     int n[2];   // query tile t visits key tiles lo[t] .. n[t]-1 (n = 0: tile is past Tq)
     int lo[2];  // first key tile holding a key of the tile's first row's window
+    int split;  // key split (0 without splits)
     int q0, k0, Tq, Tk;  // packed mode only
 };
 
@@ -162,7 +171,12 @@ template <bool kPacked>
 __device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p, const Record& rec) {
     Item it;
     int Tq, Tk;
+    it.split = 0;
     if constexpr (!kPacked) {
+        if (p.splits > 1) {
+            it.split = idx % p.splits;
+            idx /= p.splits;
+        }
         const int qrev = idx / p.n_bh;
         it.bh = idx - qrev * p.n_bh;
         it.qb = p.n_qblocks - 1 - qrev;
@@ -195,6 +209,10 @@ __device__ __forceinline__ Item decode_item(int idx, const PrefillParams& p, con
             it.n[t] = kmax / BN + 1;
         } else {
             it.n[t] = (Tk + BN - 1) / BN;
+        }
+        if (!kPacked && p.splits > 1 && it.n[t] > 0) {  // this split's key tiles
+            it.lo[t] = it.split * p.tiles_per_split;
+            it.n[t] = min(it.n[t], it.lo[t] + p.tiles_per_split);
         }
     }
     return it;
@@ -702,6 +720,15 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                     const int64_t orow =
                         kPacked ? static_cast<int64_t>(it.q0 + row[r]) * p.Hq + it.bh
                                 : static_cast<int64_t>(it.bh) * p.Tq + row[r];
+                    if (!kPacked && p.splits > 1) {  // this split's partial output, fp32
+                        float2* wptr = reinterpret_cast<float2*>(
+                            p.ws_o + (orow * p.splits + it.split) * D + 64 * c + kq);
+#pragma unroll
+                        for (int n = 0; n < 8; ++n)
+                            wptr[4 * n] = make_float2(__uint_as_float(ov[4 * n + 2 * r]) * inv[r],
+                                                      __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
+                        continue;
+                    }
                     uint32_t* optr =
                         reinterpret_cast<uint32_t*>(p.o + orow * D + 64 * c + kq);
 #pragma unroll
@@ -711,7 +738,15 @@ __device__ void softmax_group(Bars* bars, uint32_t tmem, const PrefillParams& p,
                                                __uint_as_float(ov[4 * n + 2 * r + 1]) * inv[r]);
                 }
             }
-            if ((lane & 3) == 0 && p.lse != nullptr) {
+            if (!kPacked && p.splits > 1) {  // the split's base-2 log-sum-exp
+                if ((lane & 3) == 0) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+                        if (row[r] < Tq)
+                            p.ws_lse[(static_cast<int64_t>(it.bh) * p.Tq + row[r]) * p.splits +
+                                     it.split] = st[t].m[r] + __log2f(l[r]);
+                }
+            } else if ((lane & 3) == 0 && p.lse != nullptr) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
                     if (row[r] < Tq)
@@ -980,7 +1015,18 @@ cudaError_t launch_prefill_bf16(const PrefillMaps& maps, uint16_t* o, float* lse
     prm.scale_log2 = s.scale * 1.4426950408889634f;
     prm.n_qblocks = (s.Tq + kItemRows - 1) / kItemRows;
     prm.n_bh = s.B * s.Hq;
-    const long long items = static_cast<long long>(prm.n_qblocks) * prm.n_bh;
+    // Key splits (non-causal, no window; the caller checks): every split gets
+    // at least one key tile.
+    prm.splits = 1;
+    prm.tiles_per_split = 0;
+    prm.ws_o = s.split_o;
+    prm.ws_lse = s.split_lse;
+    if (s.kv_splits > 1) {
+        const int tiles = (s.Tk + BN - 1) / BN;
+        prm.tiles_per_split = (tiles + s.kv_splits - 1) / s.kv_splits;
+        prm.splits = (tiles + prm.tiles_per_split - 1) / prm.tiles_per_split;
+    }
+    const long long items = static_cast<long long>(prm.n_qblocks) * prm.n_bh * prm.splits;
     if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     prm.n_items = static_cast<int>(items);
     prm.items = nullptr;
@@ -1017,6 +1063,10 @@ cudaError_t launch_prefill_packed_bf16(const PrefillMaps& maps, uint16_t* o, flo
     prm.items = sched.items;
     prm.n_items_dev = sched.n_items;
     prm.total_q = s.total_q;
+    prm.splits = 1;
+    prm.tiles_per_split = 0;
+    prm.ws_o = nullptr;
+    prm.ws_lse = nullptr;
     prm.status = env.status;
     prm.limit_ns = env.wait_limit_ns;
     const int grid = sched.item_bound < env.num_sms ? sched.item_bound : env.num_sms;
