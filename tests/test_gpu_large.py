@@ -47,6 +47,34 @@ def test_prefill_with_q_beyond_2_31_elements():
     _check_rows(o, lse, q, k, v, True, picks, "prefill T=262144")
 
 
+def test_d64_prefill_with_q_beyond_2_31_elements():
+    """The head-dim-64 kernel (TMA-stored O, one query tile per item)."""
+    a = attn()
+    B, Hq, Hkv, T, D = 1, 128, 8, 262144, 64   # q, o: 2^31 elements each
+    assert B * Hq * T * D >= BIG
+    q, k, v = _randn((B, Hq, T, D), 21), _randn((B, Hkv, T, D), 22), _randn((B, Hkv, T, D), 23)
+    o, lse = a.attn_fwd(q, k, v, causal=True)
+    check_status(a)
+    rng = np.random.default_rng(1)
+    picks = [(0, 127, T - 1), (0, 127, T - 17), (0, 64, 131072), (0, 0, 3)] + \
+            [(0, int(rng.integers(Hq)), int(rng.integers(T))) for _ in range(6)]
+    _check_rows(o, lse, q, k, v, True, picks, "D=64 prefill T=262144")
+
+
+def test_group_decode_key_ranges_with_kv_beyond_2_31_elements():
+    """Eight query heads per KV head and one batch row: key ranges on the
+    prefill kernel over 2^31-element K and V, merged by the combine kernel."""
+    a = attn()
+    B, Hq, Hkv, Tk, D = 1, 64, 8, 1 << 21, 128   # k, v: 2^31 elements each
+    assert B * Hkv * Tk * D >= BIG
+    q, k, v = _randn((B, Hq, 1, D), 24), _randn((B, Hkv, Tk, D), 25), _randn((B, Hkv, Tk, D), 26)
+    o, lse = a.attn_fwd(q, k, v, causal=False)
+    _, ranges, kernels = a.last_launch_info()
+    check_status(a)
+    assert ranges > 1 and kernels == 2
+    _check_rows(o, lse, q, k, v, False, [(0, 63, 0), (0, 0, 0), (0, 29, 0)], "key ranges Tk=2^21")
+
+
 def test_decode_with_kv_beyond_2_31_elements():
     a = attn()
     B, Hq, Hkv, Tk, D = 128, 32, 8, 16384, 128   # k, v: 2^31 elements each
