@@ -127,8 +127,8 @@ attn_status attn_fwd_prefill(const void* q, const void* k, const void* v,
  * KV head, automatic mode instead runs the tensor-core prefill kernel: the
  * query heads that share a KV head are the rows of a non-causal prefill
  * against its keys (q viewed as [B, Hkv, Hq/Hkv, D]), P rounded to bf16 for
- * the tensor cores as in attn_fwd_prefill.  For bf16 at D = 128, when the
- * B*Hkv pairs fill at most half the SMs, each pair's keys are cut into
+ * the tensor cores as in attn_fwd_prefill.  At D = 128, when the B*Hkv
+ * pairs fill at most half the SMs, each pair's keys are cut into
  * ranges of at least two 128-key tiles, one work item each, whose partials
  * are merged like the split ranges below (the range count is reported as
  * attn_last_launch_info's items); otherwise one work item per pair, with no

@@ -75,12 +75,12 @@ def test_gqa8_decode_full(seed):
 
 def _group_route(B, Hq, Hkv, Tk, D, dtype, sms):
     """The automatic decode route for 8 or more query heads per KV head, as
-    the library states it: key ranges on the prefill kernel (bf16, D=128,
+    the library states it: key ranges on the prefill kernel (D=128,
     (b, hkv) pairs filling at most half the SMs, two key tiles per range),
     else the prefill kernel per (b, hkv) from B*Hq >= 512 rows on, else the
     CUDA-core stream-K kernel."""
     pairs, tiles = B * Hkv, -(-Tk // 128)
-    if dtype == "bf16" and D == 128 and 2 * pairs <= sms:
+    if D == 128 and 2 * pairs <= sms:
         splits = min(sms // pairs, tiles // 2)
         if splits >= 2:
             per = -(-tiles // splits)
@@ -99,8 +99,9 @@ def _group_route(B, Hq, Hkv, Tk, D, dtype, sms):
     (1, 512, 1, 2048, 128, "bf16"),   # 512 query heads: two query blocks per range
     (16, 64, 8, 700, 128, "bf16"),    # 128 pairs: one item per (b, hkv)
     (4, 128, 8, 3001, 64, "bf16"),    # D=64 (two CTAs per SM), one item per (b, hkv)
-    (8, 64, 8, 700, 128, "f16"),      # fp16: one item per (b, hkv)
-    (2, 64, 8, 1000, 128, "f16"),     # fp16 with few rows: the CUDA-core kernel
+    (16, 64, 8, 700, 128, "f16"),     # fp16: one item per (b, hkv)
+    (2, 64, 8, 1000, 128, "f16"),     # fp16 with few rows: key ranges
+    (2, 64, 8, 1000, 64, "bf16"),     # D=64 with few rows: the CUDA-core kernel
 ])
 def test_many_heads_per_kv_head_decode(B, Hq, Hkv, Tk, D, dtype):
     a = attn()

@@ -301,12 +301,12 @@ attn_status run_decode_as_prefill(const void* q, const void* k, const void* v, v
 // With few (b, hkv) the same prefill leaves SMs idle, so its keys are cut
 // into ranges: each (b, hkv, range) is one work item writing a normalised
 // partial output and its log-sum-exp, and the split decode's combine kernel
-// merges the ranges ("3.3 Self-Attention机制深入理解" §12.3).  Taken for bf16 at
-// D = 128 with 8 or more query heads per KV head when the (b, hkv) pairs fill
-// fewer than half the SMs and each range still holds two key tiles; returns
-// the range count (every range non-empty), or 1 when not taken.
+// merges the ranges ("3.3 Self-Attention机制深入理解" §12.3).  Taken at D = 128
+// (bf16 or fp16) with 8 or more query heads per KV head when the (b, hkv)
+// pairs fill at most half the SMs and each range still holds two key tiles;
+// returns the range count (every range non-empty), or 1 when not taken.
 int decode_group_splits(const Shape& s, int num_sms) {
-    if (s.f16 || s.D != 128 || s.Hq / s.Hkv < 8) return 1;
+    if (s.D != 128 || s.Hq / s.Hkv < 8) return 1;
     const long long pairs = static_cast<long long>(s.B) * s.Hkv;
     if (2 * pairs > num_sms) return 1;
     const int tiles = (s.Tk + 127) / 128;
@@ -327,6 +327,7 @@ attn_status run_decode_as_split_prefill(const void* q, const void* k, const void
                                         const LaunchEnv& env) {
     Shape p{s.B, s.Hkv, s.Hkv, s.Hq / s.Hkv, s.Tk, s.D, 0, s.scale};
     const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+    p.f16 = s.f16;
     p.kv_splits = splits;
     p.split_o = static_cast<float*>(ws);
     p.split_lse = p.split_o + rows * splits * s.D;
@@ -334,7 +335,7 @@ attn_status run_decode_as_split_prefill(const void* q, const void* k, const void
     if (st != ATTN_OK) return st;
     const int grid = t_last_grid;
     cudaError_t e = launch_decode_combine(p.split_o, p.split_lse, static_cast<uint16_t*>(o), lse,
-                                          static_cast<int>(rows), s.D, splits, env);
+                                          static_cast<int>(rows), s.D, splits, s.f16 != 0, env);
     if (e != cudaSuccess) return cuda_fail(e, "decode combine launch");
     record_launch(grid, splits, 2);
     return ok();

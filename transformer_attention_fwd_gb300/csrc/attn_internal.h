@@ -95,9 +95,9 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
                                const Shape& s, int splits, const LaunchEnv& env,
                                int* kernels_launched);
 // The merge of split partials alone (ws_o [rows, splits, D], ws_lse [rows,
-// splits] base 2) into bf16 O and lse (may be null).
+// splits] base 2) into bf16 (f16: fp16) O and lse (may be null).
 cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16_t* o, float* lse,
-                                  int rows, int D, int splits, const LaunchEnv& env);
+                                  int rows, int D, int splits, bool f16, const LaunchEnv& env);
 int decode_choose_splits(const Shape& s, int num_sms);
 
 // Stream-K decode: one persistent CTA per SM over equal slices of all keys;

@@ -338,7 +338,7 @@ decode_split_kernel(const DecodeParams p) {
 
 // Merge the splits of one (b, hq): lse = log sum_s e^{lse_s},
 // O = sum_s e^{lse_s - lse} O_s (all in base 2 internally).
-template <int D>
+template <int D, bool kF16 = false>
 __global__ void __launch_bounds__(D)
 decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
                       uint16_t* __restrict__ o, float* __restrict__ lse, int splits) {
@@ -355,7 +355,7 @@ decode_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ 
     float acc = 0.0f;
     const float* op = ws_o + row * splits * D + d;
     for (int s = 0; s < splits; ++s) acc = fmaf(s_w[s], op[static_cast<int64_t>(s) * D], acc);
-    const uint32_t pk = pack_bf16x2(acc / L, 0.0f);
+    const uint32_t pk = Elem16<kF16>::pack(acc / L, 0.0f);
     o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
     if (d == 0 && lse != nullptr) lse[row] = (M + __log2f(L)) * kLn2;
 }
@@ -467,12 +467,18 @@ cudaError_t launch_decode_bf16(const uint16_t* q, const uint16_t* k, const uint1
 }
 
 cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16_t* o, float* lse,
-                                  int rows, int D, int splits, const LaunchEnv& env) {
+                                  int rows, int D, int splits, bool f16, const LaunchEnv& env) {
     const size_t sh = static_cast<size_t>(splits) * sizeof(float);
-    if (D == 64)
+    if (f16) {
+        if (D == 64)
+            decode_combine_kernel<64, true><<<rows, 64, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
+        else
+            decode_combine_kernel<128, true><<<rows, 128, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
+    } else if (D == 64) {
         decode_combine_kernel<64><<<rows, 64, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
-    else
+    } else {
         decode_combine_kernel<128><<<rows, 128, sh, env.stream>>>(ws_o, ws_lse, o, lse, splits);
+    }
     return cudaGetLastError();
 }
 
