@@ -451,7 +451,8 @@ def run_secondary(args, attn, peaks, flush):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(gbs / hbm, 4),
                      "traffic": load_traffic("paged_decode_b64_tk4096_p16", DECODE_SOURCES),
-                     "note": "step time includes the length prefix, stream and combine kernels"},
+                     "note": "step time includes the stream kernel (which also sums the request "
+                             "lengths) and the fragment combine kernel"},
     }
     del q, kv, bt, sl, o, lse
     # GPT-2-small-shaped causal prefill, D = 64.

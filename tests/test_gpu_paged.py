@@ -44,6 +44,8 @@ def _check(a, q, kv, bt, sl, what):
     (2, 8, 8, 128, 16, [300, 4096]),              # MHA in 16-token blocks
     (2, 32, 8, 64, 16, [777, 2048]),              # D=64, GQA-4
     (2, 8, 4, 64, 32, [500, 31]),                 # D=64, 32-token blocks
+    (3, 8, 2, 128, 16, [0, 0, 0]),                # no request has keys
+    (4, 8, 2, 128, 16, [0, 300, 0, 5]),           # empty requests around short ones
 ])
 def test_paged_matches_oracle(B, Hq, Hkv, D, page, lens):
     a = attn()
@@ -68,6 +70,23 @@ def test_many_short_requests_gqa():
     lens = rng.integers(1, 200, size=80)
     q, kv, bt, sl = make_paged(80, 16, 8, 128, 16, lens, seed=17)
     _check(a, q, kv, bt, sl, "80 short GQA requests")
+
+
+@pytest.mark.parametrize("B", [1024, 1025, 1500])
+def test_length_prefix_in_the_kernel_and_in_a_prefix_kernel(B):
+    """Up to 1024 requests every CTA sums the lengths itself (two kernels: the
+    stream kernel and the combine); more take a prefix kernel first."""
+    a = attn()
+    rng = np.random.default_rng(B)
+    lens = rng.integers(0, 120, size=B)
+    lens[::97] = 0
+    q, kv, bt, sl = make_paged(B, 4, 2, 64, 16, lens, seed=B)
+    _check(a, q, kv, bt, sl, f"{B} requests")
+    _, _, kernels = a.last_launch_info()
+    assert kernels == (2 if B <= 1024 else 3)
+    sl[B // 2] = -1  # a bad length is reported on both paths
+    a.attn_fwd_decode_paged(*to_dev(q, kv, bt, sl))
+    assert a.device_status() == a.ATTN_ERR_BAD_INPUT
 
 
 @pytest.mark.parametrize("seed", [0, 1])

@@ -498,9 +498,28 @@ cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16
 namespace {
 
 constexpr int kStreamWarps = 8;
-constexpr int kStreamThreads = (kStreamWarps + 1) * 32;  // + one producer warp
+// Producer warps: the dense cache needs one lane of one; the paged cache's
+// per-block copies take all of them, on alternate chunks.
+constexpr int kProducerWarps = 2;
+constexpr int kStreamThreads = (kStreamWarps + kProducerWarps) * 32;
 constexpr int kStageBytes = 32 * 1024;                   // K half + V half
 constexpr int kStreamStages = 5;
+// Paged mode: up to this many requests, every CTA computes the prefix of the
+// request lengths itself, in shared memory; more run a prefix kernel first.
+constexpr int kMaxPrefixB = 1024;
+
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start while the grid before it in the stream is still
+// running.  It must wait for that grid (and its memory operations) before
+// reading what the grid wrote; in a grid launched without the attribute the
+// wait returns at once.  The earlier grid signals that its dependants may be
+// scheduled once all its CTAs are resident.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 enum : unsigned { SITE_DEC_FULL = 40, SITE_DEC_EMPTY, SITE_DEC_SEG };
 
@@ -510,9 +529,17 @@ enum : unsigned { SITE_DEC_FULL = 40, SITE_DEC_EMPTY, SITE_DEC_SEG };
 struct PagedParams {
     const uint16_t* kv;          // [num_blocks, 2, Hkv, page, D], 0 = K, 1 = V
     const int32_t* block_table;  // [B, max_pages]
-    const long long* cum;        // [B + 1] keys of requests 0..b-1 (prefix kernel)
-    const long long* geom;       // [2] total virtual keys, keys per CTA
+    const int32_t* seq_lens;     // [B] keys of each request
+    // [B + 1] keys of requests 0..b-1 and [2] total virtual keys, keys per
+    // CTA: written by the prefix kernel (in_kernel == 0) or, when every CTA
+    // computes them itself (in_kernel == 1), by CTA 0 for the combine kernel.
+    long long* cum;
+    long long* geom;
+    // [grid] for CTA c >= 1: the unit its slice starts in, {b, hkv * chunks +
+    // chunk, offset of the slice start in the unit, unit length} (combine).
+    int4* first_unit;
     int B, page, max_pages, num_blocks;
+    int in_kernel;
 };
 
 struct StreamParams {
@@ -534,10 +561,11 @@ struct StreamParams {
 struct StreamBars {
     uint64_t full[kStreamStages], empty[kStreamStages];
     uint64_t seg_in, seg_out;
+    long long scan[32];  // paged mode: per-warp totals of the length prefix
     int abort;
 };
 
-template <int D, int HC>
+template <int D, int HC, bool kPaged = false>
 struct StreamLayout {
     static constexpr int LPK = D / 8;
     static constexpr int KPL = 32 / LPK;
@@ -551,7 +579,8 @@ struct StreamLayout {
     static constexpr int kMOff = kPOff + kStreamWarps * KPL * NV0 * 4;
     static constexpr int kLOff = kMOff + kStreamWarps * HC * 4;
     static constexpr int kBarOff = (kLOff + kStreamWarps * HC * 4 + 15) / 16 * 16;
-    static constexpr int kBytes = kBarOff + static_cast<int>(sizeof(StreamBars)) + 128;
+    static constexpr int kCumOff = (kBarOff + static_cast<int>(sizeof(StreamBars)) + 15) / 16 * 16;
+    static constexpr int kBytes = kCumOff + (kPaged ? (kMaxPrefixB + 1) * 8 : 0) + 128;
 };
 
 // One unit (request b, KV head hkv, head chunk) fragment [k0, k1) of its L
@@ -583,10 +612,10 @@ __device__ __forceinline__ bool next_segment(long long& v, long long v1, const S
 // The same with per-request lengths: request b's units start at
 // cum[b] * (Hkv * chunks), each L_b = cum[b + 1] - cum[b] keys long.
 __device__ __forceinline__ bool next_segment_paged(long long& v, long long v1,
-                                                   const StreamParams& p, Segment& sg) {
+                                                   const StreamParams& p, const long long* cum,
+                                                   Segment& sg) {
     if (v >= v1) return false;
     const long long U = static_cast<long long>(p.Hkv) * p.chunks;
-    const long long* cum = p.pg.cum;
     int lo = 0, hi = p.pg.B - 1;  // last request whose first unit starts at or before v
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -611,16 +640,68 @@ __device__ __forceinline__ bool next_segment_paged(long long& v, long long v1,
 // outside it is reported in the status word and block 0 is used instead, so
 // the copy stays inside the pool and the stage still receives the bytes its
 // barrier expects.
-__device__ __forceinline__ int paged_block_id(const StreamParams& p, int b, int page) {
-    int blk = p.pg.block_table[static_cast<int64_t>(b) * p.pg.max_pages + page];
+__device__ __forceinline__ int paged_block_id_load(const StreamParams& p, int b, int page) {
+    return p.pg.block_table[static_cast<int64_t>(b) * p.pg.max_pages + page];
+}
+__device__ __forceinline__ int paged_block_id_check(const StreamParams& p, int blk) {
     if (blk < 0 || blk >= p.pg.num_blocks) {
         atomicOr(p.status, ATTN_DEV_BAD_INPUT);
         blk = 0;
     }
     return blk;
 }
+__device__ __forceinline__ int paged_block_id(const StreamParams& p, int b, int page) {
+    return paged_block_id_check(p, paged_block_id_load(p, b, page));
+}
 
-// Nine warps put three on one SM sub-partition, whose 16K registers cap a
+// Paged mode, every CTA: cum[b] = keys of requests 0..b-1 in shared memory
+// (B <= kMaxPrefixB), with each length clamped into 0 .. max_pages * page
+// (CTA 0 reports a length outside it in the status word).  Every thread of
+// the CTA takes part.
+__device__ void block_length_prefix(const StreamParams& p, long long* cum, long long* warp_tot) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.pg.B, max_keys = p.pg.max_pages * p.pg.page;
+    const int per = (B + nt - 1) / nt;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    long long mine = 0;
+    for (int b = b0; b < b1; ++b) {
+        int L = p.pg.seq_lens[b];
+        if (L < 0 || L > max_keys) {
+            if (blockIdx.x == 0) atomicOr(p.status, ATTN_DEV_BAD_INPUT);
+            L = L < 0 ? 0 : max_keys;
+        }
+        mine += L;
+    }
+    // Exclusive scan of the per-thread sums: within warps, then across warps.
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = lane < nt / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long run = incl - mine + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int b = b0; b < b1; ++b) {
+        cum[b] = run;
+        const int L = p.pg.seq_lens[b];
+        run += L < 0 ? 0 : (L > max_keys ? max_keys : L);
+    }
+    if (tid == nt - 1) cum[B] = run;  // the last thread's range ends at B (or is empty)
+    __syncthreads();
+}
+
+// Ten warps put three on two SM sub-partitions, whose 16K registers cap a
 // thread at 168 (HC = 8 spills a little; splitting the heads would re-read K/V).
 // kPaged: keys come from the paged cache, per-request lengths, and cut units
 // leave their fragments in per-CTA slots (first segment of the CTA: slot 0,
@@ -628,7 +709,7 @@ __device__ __forceinline__ int paged_block_id(const StreamParams& p, int b, int 
 template <int D, int HC, bool kPaged, bool kF16 = false>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 decode_stream_kernel(const StreamParams p) {
-    using L = StreamLayout<D, HC>;
+    using L = StreamLayout<D, HC, kPaged>;
     constexpr int LPK = L::LPK, KPL = L::KPL, KW = L::KW, NV0 = L::NV0, CK = L::CK;
     constexpr int NV = NV0 >= LPK ? NV0 / LPK : 1;
     constexpr int kHalf = kStageBytes / 2;
@@ -654,27 +735,70 @@ decode_stream_kernel(const StreamParams p) {
     }
     __syncthreads();
     const WaitGuard g{p.status, &bars->abort, p.limit_ns};
-    const long long total = kPaged ? p.pg.geom[0] : p.total;
-    const long long per_cta = kPaged ? p.pg.geom[1] : p.per_cta;
+    long long total = p.total, per_cta = p.per_cta;
+    const long long* cum = nullptr;
+    if constexpr (kPaged) {
+        const long long units_per_req = static_cast<long long>(p.Hkv) * p.chunks;
+        if (p.pg.in_kernel) {
+            long long* s_cum = reinterpret_cast<long long*>(smem + L::kCumOff);
+            block_length_prefix(p, s_cum, bars->scan);
+            cum = s_cum;
+            total = s_cum[p.pg.B] * units_per_req;
+            per_cta = total > 0 ? (total + gridDim.x - 1) / gridDim.x : 1;
+            if (blockIdx.x == 0) {  // for the combine kernel
+                for (int i = threadIdx.x; i <= p.pg.B; i += blockDim.x) p.pg.cum[i] = s_cum[i];
+                if (threadIdx.x == 0) {
+                    p.pg.geom[0] = total;
+                    p.pg.geom[1] = per_cta;
+                }
+            }
+        } else {
+            cum = p.pg.cum;
+            total = p.pg.geom[0];
+            per_cta = p.pg.geom[1];
+        }
+        // Requests without keys: O = 0 and lse = -inf (no slice covers them).
+        for (int b = blockIdx.x; b < p.pg.B; b += gridDim.x) {
+            if (cum[b + 1] != cum[b]) continue;
+            for (int i = threadIdx.x; i < p.Hq * D; i += blockDim.x)
+                p.o[static_cast<int64_t>(b) * p.Hq * D + i] = 0;
+            if (p.lse != nullptr)
+                for (int i = threadIdx.x; i < p.Hq; i += blockDim.x)
+                    p.lse[static_cast<int64_t>(b) * p.Hq + i] = -INFINITY;
+        }
+    }
+    grid_launch_dependents();
     const long long v_begin = static_cast<long long>(blockIdx.x) * per_cta;
     const long long v_end = v_begin + per_cta < total ? v_begin + per_cta : total;
     auto next = [&](long long& vv, Segment& sg) {
-        return kPaged ? next_segment_paged(vv, v_end, p, sg) : next_segment(vv, v_end, p, sg);
+        return kPaged ? next_segment_paged(vv, v_end, p, cum, sg) : next_segment(vv, v_end, p, sg);
     };
+    if constexpr (kPaged) {
+        if (threadIdx.x == 0 && blockIdx.x > 0) {
+            long long vv = v_begin;
+            Segment sg0;
+            if (next(vv, sg0))
+                p.pg.first_unit[blockIdx.x] =
+                    make_int4(sg0.b, sg0.hkv * p.chunks + sg0.chunk, sg0.k0, sg0.L);
+        }
+    }
 
-    if (warp == kStreamWarps && kPaged) {
-        // Producer (paged): the lanes of the warp issue a chunk's copies
-        // together.  Lane 2i copies the K rows of the chunk's page i and lane
-        // 2i+1 its V rows; each lane loads and checks its own block id, so the
-        // ids, the address arithmetic and the copies of up to 8 pages take one
-        // pass instead of a serial chain in one lane.  Pages beyond the first
-        // 8 (blocks of fewer than 8 keys) repeat the pass.  (Loading the next
+    if (warp >= kStreamWarps && kPaged) {
+        // Producers (paged): the producer warps take alternate chunks, and
+        // the lanes of a warp issue a chunk's copies together.  Lane 2i
+        // copies the K rows of the chunk's page i and lane 2i+1 its V rows;
+        // each lane loads and checks its own block id, so the ids, the
+        // address arithmetic and the copies of up to 8 pages take one pass
+        // instead of a serial chain in one lane.  Pages beyond the first 8
+        // (blocks of fewer than 8 keys) repeat the pass.  (Loading the next
         // chunk's ids while this chunk is issued measured slower: a lane's
-        // outstanding loads delay its copy issue.)  Every lane runs the
-        // same loop and waits on the stage barrier by itself: no warp-wide
-        // vote or shuffle, which would wait for the issued copies to be taken
-        // by the copy engine.
+        // outstanding loads delay its copy issue.)  Every lane runs the same
+        // loop and waits on the stage barrier by itself: no warp-wide vote or
+        // shuffle, which would wait for the issued copies to be taken by the
+        // copy engine.  Page arithmetic uses shifts for power-of-two pages.
+        const uint32_t pw = static_cast<uint32_t>(warp - kStreamWarps);
         const int P = p.pg.page;
+        const int pshift = (P & (P - 1)) == 0 ? __ffs(P) - 1 : -1;
         const int pi = lane >> 1;
         const bool is_v = (lane & 1) != 0;
         const int64_t head_rows = static_cast<int64_t>(P) * D;
@@ -687,16 +811,20 @@ decode_stream_kernel(const StreamParams p) {
             const uint16_t* seg_base = p.pg.kv + static_cast<int64_t>(sg.hkv) * head_rows +
                                        (is_v ? static_cast<int64_t>(p.Hkv) * head_rows : 0);
             for (int kc = sg.k0; kc < sg.k1; kc += CK, ++it) {
+                if (it % kProducerWarps != pw) continue;
                 const int n = min(CK, sg.k1 - kc);
                 const int s = it % kStreamStages;
-                const int pg0 = kc / P;
-                const int np = (kc + n - 1) / P - pg0 + 1;
-                int id = (lane < 16 && pi < np) ? paged_block_id(p, sg.b, pg0 + pi) : 0;
+                const int pg0 = pshift >= 0 ? kc >> pshift : kc / P;
+                const int np = (pshift >= 0 ? (kc + n - 1) >> pshift : (kc + n - 1) / P) - pg0 + 1;
+                // The block id is loaded before the stage wait and checked
+                // after it, so that the load's latency overlaps the wait.
+                int id = (lane < 16 && pi < np) ? paged_block_id_load(p, sg.b, pg0 + pi) : 0;
                 if (it >= (uint32_t)kStreamStages &&
                     !mbar_wait(&bars->empty[s], ((it / kStreamStages) & 1) ^ 1, g, SITE_DEC_EMPTY)) {
                     ok = false;
                     break;
                 }
+                if (lane < 16 && pi < np) id = paged_block_id_check(p, id);
                 uint8_t* stage = smem + L::kRingOff + s * kStageBytes;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&bars->full[s], 2u * static_cast<uint32_t>(n) * D * 2);
@@ -753,7 +881,7 @@ decode_stream_kernel(const StreamParams p) {
             }
         out:;
         }
-    } else {
+    } else if (warp < kStreamWarps) {
         const int grp = lane / LPK, sub = lane % LPK;
         uint32_t it = 0, nseg = 0;
         long long v = v_begin;
@@ -971,20 +1099,27 @@ decode_stream_kernel(const StreamParams p) {
 }
 
 // Merge the fragments of the units that slice boundaries cut; units a single
-// CTA covered were written directly.
+// CTA covered were written directly.  Block j takes the boundary at virtual
+// key (j + 1) * per_cta and merges the unit it cuts, if that is the unit's
+// first cut boundary; its hc * D threads take one (head, column) each, so
+// every load is issued at once.  Launched with programmatic stream
+// serialisation: it waits for the stream kernel before reading the fragments.
 template <int D, bool kF16 = false>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(1024)
 decode_stream_combine_kernel(const StreamParams p, int hc) {
-    const int row = blockIdx.x;
-    const int d = threadIdx.x;
-    const int b = row / p.Hq, hq = row - b * p.Hq;
-    const int hkv = hq / p.group, hl = hq - hkv * p.group;
-    const long long u = (static_cast<long long>(b) * p.Hkv + hkv) * p.chunks + hl / hc;
-    const int h = hl % hc;
-    const long long c0 = (u * p.Tk) / p.per_cta;
-    const long long c1 = (u * p.Tk + p.Tk - 1) / p.per_cta;
+    grid_dependency_wait();
+    const int d = threadIdx.x % D, h = threadIdx.x / D;
+    const long long pos = (blockIdx.x + 1LL) * p.per_cta;
+    if (pos >= p.total) return;
+    const long long u = pos / p.Tk;
+    const long long start = u * p.Tk;
+    if (start == pos || start < pos - p.per_cta) return;  // not cut here, or cut earlier
+    const long long c0 = start / p.per_cta;
+    const long long c1 = (start + p.Tk - 1) / p.per_cta;
     const int nseg = static_cast<int>(c1 - c0 + 1);
-    if (nseg == 1) return;
+    const long long pair = u / p.chunks;
+    const int chunk = static_cast<int>(u - pair * p.chunks);
+    const int b = static_cast<int>(pair / p.Hkv), hkv = static_cast<int>(pair % p.Hkv);
     float M = -INFINITY;
     for (int s = 0; s < nseg; ++s) M = fmaxf(M, p.ws_lse[(u * p.nseg_max + s) * hc + h]);
     float Ls = 0.0f, acc = 0.0f;
@@ -994,8 +1129,9 @@ decode_stream_combine_kernel(const StreamParams p, int hc) {
         Ls += w;
         acc = fmaf(w, p.ws_o[slot * D + d], acc);
     }
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + hkv * p.group + chunk * hc + h;
     const uint32_t pk = Elem16<kF16>::pack(acc / Ls, 0.0f);
-    p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
+    p.o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
 }
 
@@ -1051,47 +1187,65 @@ paged_prefix_kernel(const int32_t* seq_lens, int B, int max_keys, long long unit
     }
 }
 
-// Paged mode: merge the fragments of cut units (CTA slots) and give requests
-// without keys O = 0, lse = -inf; units one CTA covered were written directly.
+// Paged mode: merge the fragments of cut units (CTA slots; requests without
+// keys were written by the stream kernel).  Block j takes the boundary at
+// virtual key (j + 1) * per_cta, which CTA j + 1's slice starts at; that CTA
+// recorded the unit its slice starts in.  Threads and launch as in the dense
+// combine.
 template <int D, bool kF16 = false>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(1024)
 decode_paged_combine_kernel(const StreamParams p, int hc) {
-    const int row = blockIdx.x;
-    const int d = threadIdx.x;
-    const int b = row / p.Hq, hq = row - b * p.Hq;
-    const int hkv = hq / p.group, hl = hq - hkv * p.group;
-    const int chunk = hl / hc, h = hl - chunk * hc;
-    const long long L = p.pg.cum[b + 1] - p.pg.cum[b];
-    if (L == 0) {
-        p.o[static_cast<int64_t>(row) * D + d] = 0;
-        if (d == 0 && p.lse != nullptr) p.lse[row] = -INFINITY;
-        return;
-    }
-    const long long U = static_cast<long long>(p.Hkv) * p.chunks;
-    const long long start = p.pg.cum[b] * U + (static_cast<long long>(hkv) * p.chunks + chunk) * L;
-    const long long per = p.pg.geom[1];
+    grid_dependency_wait();
+    const int d = threadIdx.x % D, h = threadIdx.x / D;
+    const long long total = p.pg.geom[0], per = p.pg.geom[1];
+    const long long pos = (blockIdx.x + 1LL) * per;
+    if (pos >= total) return;
+    const int4 fu = p.pg.first_unit[blockIdx.x + 1];  // {b, unit in request, offset, length}
+    const long long k0 = fu.z, L = fu.w;
+    if (k0 == 0 || k0 > per) return;  // not cut here, or cut at an earlier boundary
+    const long long start = pos - k0;
+    const int hkv = fu.y / p.chunks;
+    const int chunk = fu.y - hkv * p.chunks;
     const long long c0 = start / per, c1 = (start + L - 1) / per;
-    if (c0 == c1) return;
+    const int first = start != c0 * per ? 1 : 0;  // CTA c0 holds the unit in its last slot
     float M = -INFINITY;
-    for (long long c = c0; c <= c1; ++c) {
-        const long long slot = 2 * c + ((c == c0 && start != c0 * per) ? 1 : 0);
-        M = fmaxf(M, p.ws_lse[slot * hc + h]);
-    }
+    for (long long c = c0; c <= c1; ++c)
+        M = fmaxf(M, p.ws_lse[(2 * c + (c == c0 ? first : 0)) * hc + h]);
     float Ls = 0.0f, acc = 0.0f;
     for (long long c = c0; c <= c1; ++c) {
-        const long long slot = (2 * c + ((c == c0 && start != c0 * per) ? 1 : 0)) * hc + h;
-        const float w = ex2_approx(p.ws_lse[slot] - M);
-        Ls += w;
-        acc = fmaf(w, p.ws_o[slot * D + d], acc);
+        const long long slot = (2 * c + (c == c0 ? first : 0)) * hc + h;
+        const float wt = ex2_approx(p.ws_lse[slot] - M);
+        Ls += wt;
+        acc = fmaf(wt, p.ws_o[slot * D + d], acc);
     }
+    const int64_t row = static_cast<int64_t>(fu.x) * p.Hq + hkv * p.group + chunk * hc + h;
     const uint32_t pk = Elem16<kF16>::pack(acc / Ls, 0.0f);
-    p.o[static_cast<int64_t>(row) * D + d] = static_cast<uint16_t>(pk & 0xffffu);
+    p.o[row * D + d] = static_cast<uint16_t>(pk & 0xffffu);
     if (d == 0 && p.lse != nullptr) p.lse[row] = (M + __log2f(Ls)) * kLn2;
+}
+
+// Launches a combine kernel (grid = slice boundaries) with programmatic
+// stream serialisation, so that it is scheduled while the stream kernel
+// before it runs.
+cudaError_t launch_combine_after_stream(void (*kern)(const StreamParams, int), int blocks,
+                                        int threads, const StreamParams& p, int hc,
+                                        cudaStream_t st) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, hc);
 }
 
 template <int D, int HC, bool kPaged = false, bool kF16 = false>
 cudaError_t launch_stream(const StreamParams& p, int grid, cudaStream_t st) {
-    using L = StreamLayout<D, HC>;
+    using L = StreamLayout<D, HC, kPaged>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1142,11 +1296,23 @@ size_t decode_stream_workspace_bytes(const Shape& s, int num_sms) {
     return slots * s.D * sizeof(float) + slots * sizeof(float) + 256;
 }
 
+// Paged workspace: cum [B + 1] and geom [2] (int64), first_unit [grid] (int4),
+// then the fragment slots' outputs [2 * grid * hc, D] and lse values.
+struct PagedWsLayout {
+    size_t geom, first_unit, ws_o, ws_lse, bytes;
+    PagedWsLayout(const PagedShape& s, int grid) {
+        const size_t frag = 2ull * grid * heads_per_cta(s.Hq / s.Hkv);
+        auto up16 = [](size_t x) { return (x + 15) / 16 * 16; };
+        geom = 8ull * (s.B + 1);
+        first_unit = up16(geom + 16);
+        ws_o = up16(first_unit + 16ull * grid);
+        ws_lse = ws_o + frag * s.D * sizeof(float);
+        bytes = ws_lse + frag * sizeof(float) + 256;
+    }
+};
+
 size_t decode_paged_workspace_bytes(const PagedShape& s, int num_sms) {
-    const int group = s.Hq / s.Hkv;
-    const int hc = heads_per_cta(group);
-    const size_t frag = 2ull * num_sms * hc;  // fragment slots
-    return 16ull * (s.B + 1 + 2) + frag * s.D * sizeof(float) + frag * sizeof(float) + 256;
+    return PagedWsLayout(s, num_sms).bytes;
 }
 
 cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
@@ -1156,12 +1322,12 @@ cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
     const int group = s.Hq / s.Hkv;
     const int hc = heads_per_cta(group);
     const int grid = env.num_sms;
-    const size_t frag = 2ull * grid * hc;
+    const PagedWsLayout lay(s, grid);
     uint8_t* base = static_cast<uint8_t*>(ws);
     long long* cum = reinterpret_cast<long long*>(base);
-    long long* geom = cum + (s.B + 1);
-    float* ws_o = reinterpret_cast<float*>(base + 16ull * (s.B + 1 + 2));
-    float* ws_lse = ws_o + frag * s.D;
+    long long* geom = reinterpret_cast<long long*>(base + lay.geom);
+    float* ws_o = reinterpret_cast<float*>(base + lay.ws_o);
+    float* ws_lse = reinterpret_cast<float*>(base + lay.ws_lse);
 
     StreamParams p{};
     p.q = q; p.k = nullptr; p.v = nullptr; p.o = o; p.lse = lse;
@@ -1171,13 +1337,21 @@ cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
     p.scale_log2 = s.scale * 1.4426950408889634f;
     p.status = env.status;
     p.limit_ns = env.wait_limit_ns;
-    p.pg.kv = kv; p.pg.block_table = block_table; p.pg.cum = cum; p.pg.geom = geom;
+    p.pg.kv = kv; p.pg.block_table = block_table; p.pg.seq_lens = seq_lens;
+    p.pg.cum = cum; p.pg.geom = geom;
+    p.pg.first_unit = reinterpret_cast<int4*>(base + lay.first_unit);
     p.pg.B = s.B; p.pg.page = s.page; p.pg.max_pages = s.max_pages; p.pg.num_blocks = s.num_blocks;
+    p.pg.in_kernel = s.B <= kMaxPrefixB ? 1 : 0;
 
-    const long long units_per_req = static_cast<long long>(s.Hkv) * p.chunks;
-    paged_prefix_kernel<<<1, 1024, 0, env.stream>>>(seq_lens, s.B, s.max_pages * s.page,
-                                                    units_per_req, grid, cum, geom, env.status);
-    cudaError_t e = cudaGetLastError();
+    int launched = 2;
+    cudaError_t e = cudaSuccess;
+    if (!p.pg.in_kernel) {
+        const long long units_per_req = static_cast<long long>(s.Hkv) * p.chunks;
+        paged_prefix_kernel<<<1, 1024, 0, env.stream>>>(seq_lens, s.B, s.max_pages * s.page,
+                                                        units_per_req, grid, cum, geom, env.status);
+        e = cudaGetLastError();
+        launched = 3;
+    }
     if (e == cudaSuccess) {
         if (s.f16)
             e = (s.D == 64) ? launch_stream_d<64, true, true>(p, hc, grid, env.stream)
@@ -1186,22 +1360,17 @@ cudaError_t launch_decode_paged_bf16(const uint16_t* q, const uint16_t* kv,
             e = (s.D == 64) ? launch_stream_d<64, true>(p, hc, grid, env.stream)
                             : launch_stream_d<128, true>(p, hc, grid, env.stream);
     }
-    if (e == cudaSuccess) {
-        const int rows = s.B * s.Hq;
-        if (s.f16) {
-            if (s.D == 64)
-                decode_paged_combine_kernel<64, true><<<rows, 64, 0, env.stream>>>(p, hc);
-            else
-                decode_paged_combine_kernel<128, true><<<rows, 128, 0, env.stream>>>(p, hc);
-        } else if (s.D == 64) {
-            decode_paged_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, hc);
-        } else {
-            decode_paged_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, hc);
-        }
-        e = cudaGetLastError();
+    if (e == cudaSuccess && grid > 1) {
+        auto kern = s.f16 ? (s.D == 64 ? decode_paged_combine_kernel<64, true>
+                                       : decode_paged_combine_kernel<128, true>)
+                          : (s.D == 64 ? decode_paged_combine_kernel<64>
+                                       : decode_paged_combine_kernel<128>);
+        e = launch_combine_after_stream(kern, grid - 1, s.D * hc, p, hc, env.stream);
+    } else {
+        --launched;
     }
     if (grid_out) *grid_out = grid;
-    if (kernels_launched) *kernels_launched = 3;
+    if (kernels_launched) *kernels_launched = launched;
     return e;
 }
 
@@ -1229,19 +1398,12 @@ cudaError_t launch_decode_stream_bf16(const uint16_t* q, const uint16_t* k, cons
         e = (s.D == 64) ? launch_stream_d<64>(p, g.hc, g.grid, env.stream)
                         : launch_stream_d<128>(p, g.hc, g.grid, env.stream);
     int launched = 1;
-    if (e == cudaSuccess && g.nseg_max > 1) {
-        const int rows = s.B * s.Hq;
-        if (s.f16) {
-            if (s.D == 64)
-                decode_stream_combine_kernel<64, true><<<rows, 64, 0, env.stream>>>(p, g.hc);
-            else
-                decode_stream_combine_kernel<128, true><<<rows, 128, 0, env.stream>>>(p, g.hc);
-        } else if (s.D == 64) {
-            decode_stream_combine_kernel<64><<<rows, 64, 0, env.stream>>>(p, g.hc);
-        } else {
-            decode_stream_combine_kernel<128><<<rows, 128, 0, env.stream>>>(p, g.hc);
-        }
-        e = cudaGetLastError();
+    if (e == cudaSuccess && g.grid > 1) {
+        auto kern = s.f16 ? (s.D == 64 ? decode_stream_combine_kernel<64, true>
+                                       : decode_stream_combine_kernel<128, true>)
+                          : (s.D == 64 ? decode_stream_combine_kernel<64>
+                                       : decode_stream_combine_kernel<128>);
+        e = launch_combine_after_stream(kern, g.grid - 1, s.D * g.hc, p, g.hc, env.stream);
         launched = 2;
     }
     if (grid_out) *grid_out = g.grid;
