@@ -31,6 +31,28 @@ def test_prefill_small_shapes(B, Hq, Hkv, Tq, Tk, D, causal):
     compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16)
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tk,dtype", [
+    (1, 32, 8, 1024, 1024, "bf16"),   # 128 work items of 8 key tiles (fewer than the SMs)
+    (1, 8, 2, 256, 8192, "bf16"),     # 8 items of 64 key tiles
+    (1, 40, 4, 777, 1500, "bf16"),    # ragged query and key tails, 160 items
+    (2, 5, 1, 100, 3000, "f16"),      # fewer rows than an item, MQA, fp16
+    (1, 19, 19, 512, 640, "bf16"),    # 38 items of 5 key tiles
+    (1, 1, 1, 128, 512, "bf16"),      # one item
+    (1, 38, 2, 1024, 1024, "bf16"),   # 152 items: one whole wave
+])
+def test_noncausal_shapes(B, Hq, Hkv, Tq, Tk, dtype):
+    """Non-causal prefill at D=128 over item counts below, at and above one
+    wave of SMs, with ragged tails: one kernel, every output compared."""
+    a = attn()
+    q, k, v = make_qkv(B, Hq, Hkv, Tq, Tk, 128, dtype, seed=Tq + Tk)
+    o, lse = a.attn_fwd(*to_dev(q, k, v), causal=False)
+    _, _, kernels = a.last_launch_info()
+    check_status(a)
+    assert kernels == 1
+    o_ref, lse_ref = oracle.attention_f64(q, k, v, False)
+    compare(o, lse, o_ref, lse_ref, TOL_O_BF16, TOL_LSE_BF16, f"non-causal {B} {Hq} {Tq} {Tk}")
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_gpt2_small_prefill_full(seed):
     """B=8, H=12, T=1024, D=64 causal: every output compared."""
