@@ -72,15 +72,16 @@ def test_many_short_requests_gqa():
     _check(a, q, kv, bt, sl, "80 short GQA requests")
 
 
-@pytest.mark.parametrize("B", [1024, 1025, 1500])
-def test_length_prefix_in_the_kernel_and_in_a_prefix_kernel(B):
+@pytest.mark.parametrize("B,D,dtype", [(1024, 64, "bf16"), (1025, 64, "bf16"), (1500, 64, "bf16"),
+                                       (1100, 128, "f16")])
+def test_length_prefix_in_the_kernel_and_in_a_prefix_kernel(B, D, dtype):
     """Up to 1024 requests every CTA sums the lengths itself (two kernels: the
     stream kernel and the combine); more take a prefix kernel first."""
     a = attn()
     rng = np.random.default_rng(B)
     lens = rng.integers(0, 120, size=B)
     lens[::97] = 0
-    q, kv, bt, sl = make_paged(B, 4, 2, 64, 16, lens, seed=B)
+    q, kv, bt, sl = make_paged(B, 4, 2, D, 16, lens, seed=B, dtype=dtype)
     _check(a, q, kv, bt, sl, f"{B} requests")
     _, _, kernels = a.last_launch_info()
     assert kernels == (2 if B <= 1024 else 3)
