@@ -29,10 +29,12 @@
 // into a shared-memory ring and eight consumer warps apply the arithmetic
 // above (with the query columns and output accumulators as packed fp32
 // pairs, two columns per f32x2 instruction).  Units cut by a slice boundary
-// leave fragments that a combine kernel merges.  The same kernel reads a
-// paged cache (kPaged: per-request lengths, block-table indirection, the
-// producer warp's lanes issuing a chunk's per-block copies together) and
-// fp16 instead of bf16 elements (kF16).
+// leave fragments that a combine kernel merges (one block per slice
+// boundary, launched so that it is scheduled while the stream kernel runs).
+// The same kernel reads a paged cache (kPaged: per-request lengths summed by
+// every CTA, block-table indirection, two producer warps on alternate chunks
+// whose lanes issue a chunk's per-block copies together) and fp16 instead of
+// bf16 elements (kF16).
 #include <cuda_runtime.h>
 #include <cmath>
 #include <cstdint>
@@ -492,8 +494,8 @@ cudaError_t launch_decode_combine(const float* ws_o, const float* ws_lse, uint16
 // boundaries is merged by the combine kernel (block-merge rule,
 // "Self-Attention机制深入理解" §12.3).  A producer warp copies each chunk of K
 // and V rows (contiguous in the cache) into a shared-memory ring with bulk
-// copies; eight compute warps consume the ring with the same arithmetic as
-// the split kernel above.
+// copies (paged cache: two producer warps, alternate chunks); eight compute
+// warps consume the ring with the same arithmetic as the split kernel above.
 // ---------------------------------------------------------------------------
 namespace {
 
